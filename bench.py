@@ -1,0 +1,458 @@
+"""Benchmark of the GEMM library: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one GEMM call D = alpha*op(A)*op(B) + beta*C on the workload's
+seeded synthetic inputs (default: BF16 8192^3, A row-major, B column-major,
+D FP32), inputs resident in HBM.  ``value`` is whole-job throughput in
+TFLOPS (2MNK / time, "GEMM on NVIDIA GPUs", section 1); ``e2e`` is the same
+metric with the host->device copy of A and B (pinned memory) and the
+device->host copy of D inside every step.  Under torchrun every rank runs an
+independent replica on its own GPU (the path needs no exchange): the time is
+the maximum over ranks and ``value`` counts the work of all ranks.
+
+``--impl reference`` times the CPU oracle (the slow plain reference) on a
+bounded sample of the same workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/s) and % of GB300 BF16/FP32 peak at 8192^3, 1 GPU"
+UNIT = "TFLOPS"
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2 (~129 MB)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "gemm_bf16_tc": "dense_gemm_08_gb300/csrc/gemm_tc.cu",
+    "sgemm_simt": "dense_gemm_08_gb300/csrc/sgemm_simt.cu",
+}
+
+
+# ------------------------------------------------------------- pure helpers
+def algorithmic_bytes(M, N, K, in_bytes, beta):
+    """Bytes the method must move: A and B once, D once, C once if beta != 0
+    ("GEMM on NVIDIA GPUs", section 2, "GEMM arithmetic intensity")."""
+    b = in_bytes * (M * K + K * N) + 4 * M * N
+    if beta != 0:
+        b += 4 * M * N
+    return b
+
+
+def roofline_tflops(flops, nbytes, peak_tflops, hbm_gbs):
+    """min(peak, I * BW) in TFLOP/s, I = flops / bytes."""
+    intensity = flops / nbytes
+    return min(peak_tflops, intensity * hbm_gbs * 1e9 / 1e12)
+
+
+def fp32_core_peak_tflops(sms, mhz):
+    """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 FLOP (FMA) x clock."""
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(rel_path):
+    with open(os.path.join(ROOT, rel_path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None if there is none or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    m_src = re.search(r"^source_sha256_16:\s*([0-9a-f]+)", text, re.M)
+    if not m_bytes or not m_src:
+        return None
+    if m_src.group(1) != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return float(m_bytes.group(1))
+
+
+def clock_summary(rows):
+    """rows: parsed nvidia-smi CSV samples -> clocks object of the JSON line."""
+    if not rows:
+        return None
+    sm = [r["sm"] for r in rows if r["sm"] is not None]
+    max_mhz = max((r["max"] for r in rows if r["max"] is not None), default=None)
+    loaded = [r["sm"] for r in rows if r["sm"] is not None and r["power"] is not None
+              and r["power"] > 0.3 * max(x["power"] for x in rows if x["power"] is not None)]
+    reasons = set()
+    for r in rows:
+        reasons.update(r["reasons"])
+    return {"sm_mhz": statistics.median(loaded or sm) if sm else None, "sm_max_mhz": max_mhz,
+            "reasons": sorted(reasons), "samples": len(rows)}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+
+            def num(x):
+                try:
+                    return float(x)
+                except ValueError:
+                    return None
+            reasons = [n for n, v in zip(self.NAMES, parts[5:9]) if v.lower() == "active"]
+            self.rows.append({"sm": num(parts[1]), "max": num(parts[2]), "power": num(parts[3]),
+                              "reasons": reasons})
+        return False
+
+
+# ----------------------------------------------------------------- our arm
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, ws, device):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws, device=None):
+    if ws > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None):
+    """Time the oracle on whole rows of D (bounded sample).  Returns the JSON object."""
+    import numpy as np
+    import oracle
+
+    def bits(t):
+        if t is None:
+            return None
+        t = t.contiguous()
+        if t.dtype.is_floating_point and t.element_size() == 2:
+            import torch
+            return t.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+        return t.numpy().reshape(-1)
+
+    A, B, C = bits(inp["A"]), bits(inp["B"]), bits(inp["C"])
+    threads = oracle.default_threads()
+
+    def rows_run(r0, nrows):
+        I = np.repeat(np.arange(r0, r0 + nrows, dtype=np.int64), w.N)
+        J = np.tile(np.arange(w.N, dtype=np.int64), nrows)
+        t0 = time.perf_counter()
+        D, S = oracle.gemm_points(w.M, w.N, w.K, w.alpha, A, inp["lda"], w.order_a, B,
+                                  inp["ldb"], w.order_b, w.beta, C, inp["ldc"], w.order_cd, I, J)
+        return time.perf_counter() - t0, D, S
+
+    # calibrate on one row per thread, then size the sample to ~target_s
+    cal_rows = min(w.M, max(1, threads))
+    dt, _, _ = rows_run(0, cal_rows)
+    per_row = dt / cal_rows
+    rows = int(max(1, min(w.M, target_s / max(per_row, 1e-9))))
+    if max_rows is not None:
+        rows = min(rows, max_rows)
+    dt, D, S = rows_run(0, rows)
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of D ({rows} x {w.N} entries, K = {w.K}), "
+                      f"{dt:.2f} s", "seconds": dt, "_rows": rows, "_D": D, "_S": S}
+
+
+def bench_ours(args):
+    import torch
+    import dense_gemm_08_gb300 as lib
+    from dense_gemm_08_gb300.inputs import WORKLOADS, make_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=0)
+    fn = lib.gemm_f32 if w.dtype == "f32" else lib.gemm_bf16_f32acc
+    in_bytes = 4 if w.dtype == "f32" else 2
+
+    A = inp["A"].to(device)
+    B = inp["B"].to(device)
+    C = inp["C"].to(device) if inp["C"] is not None else None
+    D = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fn(w.M, w.N, w.K, w.alpha, A, inp["lda"], w.order_a, B, inp["ldb"], w.order_b, w.beta,
+           C, inp["ldc"], D, w.N, w.order_cd, stream)
+        return lib.gemm_last_kernel()
+
+    working_set = A.numel() * A.element_size() + B.numel() * B.element_size() + D.numel() * 4
+    if C is not None:
+        working_set += C.numel() * 4
+    flush = working_set < 2 * L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
+
+    for _ in range(args.warmup):
+        kernel = step()
+    torch.cuda.synchronize(device)
+    assert lib.gemm_last_device_status(stream) == lib.GEMM_OK
+
+    launches = 0
+    kernel_names = set()
+    with ClockSampler(local) as clocks:
+        barrier(ws, device)
+        torch.cuda.synchronize(device)
+        if flush:
+            # time each step alone, rewriting 256 MiB between steps to evict L2
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for s0, s1 in evs:
+                scratch.fill_(1.0)
+                s0.record(stream)
+                kernel_names.add(step())
+                s1.record(stream)
+                launches += 1
+            torch.cuda.synchronize(device)
+            elapsed_ms = sum(a.elapsed_time(b) for a, b in evs)
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                kernel_names.add(step())
+                launches += 1
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            elapsed_ms = e0.elapsed_time(e1)
+        barrier(ws, device)
+    assert lib.gemm_last_device_status(stream) == lib.GEMM_OK
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, device)
+    ms_per_step = elapsed_ms / args.steps
+    tflops = ws * w.flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hA = inp["A"].pin_memory()
+        hB = inp["B"].pin_memory()
+        hC = inp["C"].pin_memory() if inp["C"] is not None else None
+        hD = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            A.copy_(hA, non_blocking=True)
+            B.copy_(hB, non_blocking=True)
+            if hC is not None:
+                C.copy_(hC, non_blocking=True)
+            step()
+            hD.copy_(D, non_blocking=True)
+
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(ws, device)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, ws, device)
+        h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if hC is not None:
+            h2d += hC.numel() * 4
+        e2e = {"value": ws * w.flops * e2e_steps / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hD.numel() * 4,
+               "ms_per_step": e2e_s * 1e3 / e2e_steps}
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return None
+
+    # ---- roofline of the dominant kernel (the only one in the timed region)
+    peaks, peak_src = load_peaks()
+    kname = kernel.split("<")[0]
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+    clk = clock_summary(getattr(clocks, "rows", []))
+    if kname == "gemm_bf16_tc":
+        timed_s = elapsed_ms * 1e-3
+        key = "bf16_tflops_sustained" if timed_s > 1.0 else "bf16_tflops"
+        peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
+        peak_note = f"{peak_src} cuBLAS bf16 {'sustained' if key.endswith('sustained') else 'burst'}"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": peak_note}
+    else:
+        max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak = fp32_core_peak_tflops(sms, max_mhz)
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"FP32 FMA peak {sms} SMs x 128 lanes x 2 x {max_mhz:.0f} MHz"}
+        if clk and clk.get("sm_mhz"):
+            roof["peak_at_run_clock"] = fp32_core_peak_tflops(sms, clk["sm_mhz"])
+            roof["frac_at_run_clock"] = achieved / roof["peak_at_run_clock"]
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg = algorithmic_bytes(w.M, w.N, w.K, in_bytes, w.beta)
+    roof["algorithmic_bytes"] = alg
+    roof["roof_min_peak_ibw"] = roofline_tflops(w.flops, alg, peak, hbm)
+    roof["traffic"] = committed_traffic(kname, w.name)
+    roof["kernel"] = kname
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(w, inp, target_s=args.cpu_seconds)
+        # the oracle's sample doubles as a parity spot check of the timed output
+        import numpy as np
+        rows = cpu.pop("_rows")
+        Dref, S = cpu.pop("_D"), cpu.pop("_S")
+        got = D[:rows].cpu().numpy().reshape(-1).astype(np.float64)
+        ref = Dref.astype(np.float32).astype(np.float64)
+        if w.dtype == "f32":
+            tol = 1e-5 * S
+            if inp["C_logical"] is not None:
+                tol = tol + 1e-6 * np.abs(w.beta * inp["C_logical"][:rows].numpy().reshape(-1))
+        else:
+            tol = 4e-3 * S + 1e-6
+        cpu["sample_max_err_over_tol"] = float(np.max(np.abs(got - ref) / np.maximum(tol, 1e-300)))
+
+    line = {
+        "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "in_dtype": w.dtype, "acc_dtype": "f32", "out_dtype": "f32",
+                   "order_a": "row" if w.order_a == 0 else "col",
+                   "order_b": "row" if w.order_b == 0 else "col",
+                   "order_cd": "row" if w.order_cd == 0 else "col",
+                   "inputs": f"seed 0, {w.dist}" + (f" sigma {w.sigma}" if w.dist == "normal" else ""),
+                   "l2": ("L2 flushed between steps (256 MiB write)" if flush else
+                          f"inputs larger than L2 (working set {working_set / 2**20:.0f} MiB)"),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "kernels": sorted(kernel_names), "clocks": clk,
+    }
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+def bench_reference(args):
+    from dense_gemm_08_gb300.inputs import WORKLOADS, make_inputs
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=0)
+    per_step = max(0.5, min(10.0, args.ref_seconds / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        run_cpu_baseline(w, inp, target_s=per_step)
+    t_total, flops_total, cores, rows_total = 0.0, 0.0, 0, 0
+    for _ in range(args.steps):
+        r = run_cpu_baseline(w, inp, target_s=per_step)
+        t_total += r["seconds"]
+        flops_total += 2.0 * r["_rows"] * w.N * w.K
+        rows_total += r["_rows"]
+        cores = r["cores"]
+    value = flops_total / t_total / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "in_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps, each whole rows of D (total {rows_total} "
+                                   f"rows x {w.N}, K = {w.K}) sized to ~{per_step:.1f} s"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_8192")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    line = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+"""Python binding of the GB300 GEMM library's C ABI (include/gemm.h).
+
+Argument marshalling only: every function here forwards to the in-tree
+CUDA library ``libdense_gemm_08_gb300.so``; all arithmetic runs in its
+kernels.  Importing this package without the built library raises at the
+first call (there is no CPU fallback).
+
+Same names as the C ABI:
+    gemm_f32, gemm_bf16_f32acc, gemm_status_string, gemm_last_device_status,
+    gemm_last_kernel
+Pointer arguments take an integer device address or a torch CUDA tensor;
+``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
+(torch's current stream).  A non-zero status raises ``GemmError``.
+
+``gemm(...)`` is a convenience wrapper for torch tensors that reads each
+operand's storage order and leading dimension from its strides.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+ROW_MAJOR = 0
+COL_MAJOR = 1
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_VALUE = 1
+GEMM_ERR_UNSUPPORTED_DEVICE = 2
+GEMM_ERR_LAUNCH = 3
+GEMM_ERR_TIMEOUT = 4
+GEMM_ERR_INTERNAL = 5
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
+EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_status_string", "gemm_last_device_status",
+            "gemm_last_kernel")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({gemm_status_string(status)})")
+        self.status = status
+
+
+def library() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {LIB_PATH} is not built; run __graft_entry__.build() "
+                    "(or python dense_gemm_08_gb300/_build.py)")
+            lib = ctypes.CDLL(LIB_PATH)
+            i64, f32, vp, ip = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+            sig = [i64, i64, i64, f32, vp, i64, ip, vp, i64, ip, f32, vp, i64, vp, i64, ip, vp]
+            lib.gemm_f32.argtypes = sig
+            lib.gemm_f32.restype = ip
+            lib.gemm_bf16_f32acc.argtypes = sig
+            lib.gemm_bf16_f32acc.restype = ip
+            lib.gemm_status_string.argtypes = [ip]
+            lib.gemm_status_string.restype = ctypes.c_char_p
+            lib.gemm_last_device_status.argtypes = [vp]
+            lib.gemm_last_device_status.restype = ip
+            lib.gemm_last_kernel.argtypes = []
+            lib.gemm_last_kernel.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _addr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()  # torch tensor
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def _call(fn_name, M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
+          order_cd, stream, check):
+    fn = getattr(library(), fn_name)
+    st = fn(int(M), int(N), int(K), float(alpha), _addr(A), int(lda), int(order_a), _addr(B),
+            int(ldb), int(order_b), float(beta), _addr(C), int(ldc), _addr(D), int(ldd),
+            int(order_cd), _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, fn_name)
+    return st
+
+
+def gemm_f32(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd, order_cd,
+             stream=None, check=True) -> int:
+    """FP32 GEMM on the CUDA cores (see include/gemm.h)."""
+    return _call("gemm_f32", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                 ldd, order_cd, stream, check)
+
+
+def gemm_bf16_f32acc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
+                     order_cd, stream=None, check=True) -> int:
+    """BF16-input, FP32-accumulate GEMM (tensor cores when TMA applies; see include/gemm.h)."""
+    return _call("gemm_bf16_f32acc", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                 ldc, D, ldd, order_cd, stream, check)
+
+
+def gemm_status_string(status: int) -> str:
+    return library().gemm_status_string(int(status)).decode()
+
+
+def gemm_last_device_status(stream=None) -> int:
+    return int(library().gemm_last_device_status(_stream(stream)))
+
+
+def gemm_last_kernel() -> str:
+    return library().gemm_last_kernel().decode()
+
+
+# ------------------------------------------------------------ torch helper
+def storage_order(t):
+    """(order, ld) of a 2-D tensor, from its strides; raises if neither dense-row nor dense-column."""
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    r, q = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 and (s0 >= max(q, 1) or r <= 1):
+        return ROW_MAJOR, max(s0, q, 1)
+    if s0 == 1 and (s1 >= max(r, 1) or q <= 1):
+        return COL_MAJOR, max(s1, r, 1)
+    raise ValueError(f"tensor with strides {t.stride()} is neither row- nor column-major")
+
+
+def gemm(A, B, C=None, alpha=1.0, beta=0.0, out=None, stream=None):
+    """D = alpha * A @ B + beta * C for torch CUDA tensors.
+
+    A (M x K) and B (K x N) are float32 (-> gemm_f32) or bfloat16
+    (-> gemm_bf16_f32acc); C and the result are float32 and share one order
+    (``out``'s if given, else C's, else row-major).  Any row- or
+    column-major view works (e.g. ``B.t()`` of a contiguous N x K tensor).
+    """
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must share a dtype")
+    oa, lda = storage_order(A)
+    ob, ldb = storage_order(B)
+    if out is None:
+        if C is not None and C.shape == (M, N):
+            ocd_pref = storage_order(C)[0]
+        else:
+            ocd_pref = ROW_MAJOR
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        if ocd_pref == COL_MAJOR:
+            out = torch.empty((N, M), dtype=torch.float32, device=A.device).t()
+    ocd, ldd = storage_order(out)
+    ldc = ldd
+    if beta != 0.0:
+        if C is None:
+            raise ValueError("beta != 0 needs C")
+        oc, ldc = storage_order(C)
+        if oc != ocd:
+            raise ValueError("C and the output must share a storage order")
+    fn = gemm_f32 if A.dtype == torch.float32 else gemm_bf16_f32acc
+    if A.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("A and B must be float32 or bfloat16")
+    fn(M, N, K, alpha, A, lda, oa, B, ldb, ob, beta, C if beta != 0.0 else None, ldc, out, ldd,
+       ocd, stream)
+    return out

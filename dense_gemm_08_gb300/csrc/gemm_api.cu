@@ -1,0 +1,174 @@
+// gemm_api.cu -- the C ABI of include/gemm.h: argument checks, layout
+// normalisation and dispatch to the kernels.
+//
+// Normalisation: kernels only produce row-major D.  A column-major D is the
+// row-major Dᵀ = op(B)ᵀ op(A)ᵀ (transpose identity of the GEMM definition,
+// "GEMM on NVIDIA GPUs", section 1), so the call is rewritten with M and N
+// swapped, A and B exchanged and each operand's storage order flipped.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "gemm.h"
+#include "internal.h"
+
+#define GEMM_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local const char *t_last_kernel = "";
+
+constexpr int64_t kMaxDim = 0x7fffffff;
+
+bool is_order(gemm_order_t o) { return o == GEMM_ROW_MAJOR || o == GEMM_COL_MAJOR; }
+
+bool aligned(const void *p, size_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) % bytes) == 0;
+}
+
+int64_t need_ld(gemm_order_t order, int64_t rows, int64_t cols) {
+    const int64_t v = order == GEMM_ROW_MAJOR ? cols : rows;
+    return v > 1 ? v : 1;
+}
+
+// Every rule of the contract in gemm.h, checked before any CUDA call.
+gemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                       gemm_order_t oa, const void *B, int64_t ldb, gemm_order_t ob, float beta,
+                       const float *C, int64_t ldc, const float *D, int64_t ldd, gemm_order_t ocd,
+                       size_t in_bytes) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_VALUE;
+    if (!is_order(oa) || !is_order(ob) || !is_order(ocd)) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (D == nullptr || !aligned(D, sizeof(float)) || ldd < need_ld(ocd, M, N))
+        return GEMM_ERR_INVALID_VALUE;
+    if (beta != 0.f && (C == nullptr || !aligned(C, sizeof(float)) || ldc < need_ld(ocd, M, N)))
+        return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && alpha != 0.f) {
+        if (A == nullptr || B == nullptr || !aligned(A, in_bytes) || !aligned(B, in_bytes))
+            return GEMM_ERR_INVALID_VALUE;
+        if (lda < need_ld(oa, M, K) || ldb < need_ld(ob, K, N)) return GEMM_ERR_INVALID_VALUE;
+    }
+    return GEMM_OK;
+}
+
+gemm::Problem normalise(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                        gemm_order_t oa, const void *B, int64_t ldb, gemm_order_t ob, float beta,
+                        const float *C, int64_t ldc, float *D, int64_t ldd, gemm_order_t ocd) {
+    gemm::Problem p;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = beta != 0.f ? C : nullptr;
+    p.ldc = ldc;
+    p.D = D;
+    p.ldd = ldd;
+    if (ocd == GEMM_ROW_MAJOR) {
+        p.M = M;
+        p.N = N;
+        p.A = A;
+        p.lda = lda;
+        p.a_kmajor = oa == GEMM_ROW_MAJOR;  // A(i,k) at A[i*lda + k]
+        p.B = B;
+        p.ldb = ldb;
+        p.b_kmajor = ob == GEMM_COL_MAJOR;  // B(k,j) at B[k + j*ldb]
+    } else {
+        // Dᵀ (N x M, row-major with ldd) = op(B)ᵀ op(A)ᵀ.
+        // A' = op(B)ᵀ: A'(j,k) = B(k,j); K-major iff B(k,j) is at B[j*ldb + k], i.e. B column-major.
+        // B' = op(A)ᵀ: B'(k,i) = A(i,k); K-major iff A(i,k) is at A[k + i*lda], i.e. A row-major.
+        p.M = N;
+        p.N = M;
+        p.A = B;
+        p.lda = ldb;
+        p.a_kmajor = ob == GEMM_COL_MAJOR;
+        p.B = A;
+        p.ldb = lda;
+        p.b_kmajor = oa == GEMM_ROW_MAJOR;
+    }
+    return p;
+}
+
+// The library carries sm_103a code only.
+gemm_status_t check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return (major == 10 && minor == 3) ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+gemm_status_t finish(cudaError_t e, const char *name) {
+    if (e == cudaSuccess) {
+        t_last_kernel = name;
+        return GEMM_OK;
+    }
+    return (e == cudaErrorInvalidValue || e == cudaErrorSymbolNotFound) ? GEMM_ERR_INTERNAL
+                                                                          : GEMM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+GEMM_API gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                int64_t lda, gemm_order_t order_a, const float *B, int64_t ldb,
+                                gemm_order_t order_b, float beta, const float *C, int64_t ldc,
+                                float *D, int64_t ldd, gemm_order_t order_cd,
+                                cudaStream_t stream) {
+    t_last_kernel = "";
+    gemm_status_t st = validate(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                                ldd, order_cd, sizeof(float));
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if ((st = check_device()) != GEMM_OK) return st;
+    const gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                                      ldc, D, ldd, order_cd);
+    const char *name = "";
+    cudaError_t e = (K == 0 || alpha == 0.f)
+                        ? gemm::launch_scale_c(p, stream, &name)
+                        : gemm::launch_simt(p, gemm::InType::F32, stream, &name);
+    return finish(e, name);
+}
+
+GEMM_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
+                                        const gemm_bf16_t *A, int64_t lda, gemm_order_t order_a,
+                                        const gemm_bf16_t *B, int64_t ldb, gemm_order_t order_b,
+                                        float beta, const float *C, int64_t ldc, float *D,
+                                        int64_t ldd, gemm_order_t order_cd, cudaStream_t stream) {
+    t_last_kernel = "";
+    gemm_status_t st = validate(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                                ldd, order_cd, sizeof(gemm_bf16_t));
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if ((st = check_device()) != GEMM_OK) return st;
+    const gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                                      ldc, D, ldd, order_cd);
+    const char *name = "";
+    cudaError_t e;
+    if (K == 0 || alpha == 0.f)
+        e = gemm::launch_scale_c(p, stream, &name);
+    else if (gemm::tc_eligible(p))
+        e = gemm::launch_tc(p, stream, &name);
+    else
+        e = gemm::launch_simt(p, gemm::InType::BF16, stream, &name);
+    return finish(e, name);
+}
+
+GEMM_API const char *gemm_status_string(gemm_status_t status) {
+    switch (status) {
+        case GEMM_OK: return "success";
+        case GEMM_ERR_INVALID_VALUE: return "invalid argument (shape, leading dimension, order, NULL or misaligned pointer)";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "the current CUDA device is not sm_103";
+        case GEMM_ERR_LAUNCH: return "kernel launch failed";
+        case GEMM_ERR_TIMEOUT: return "a bounded wait in the tensor-core kernel ran out";
+        case GEMM_ERR_INTERNAL: return "internal CUDA runtime or driver error";
+    }
+    return "unknown status";
+}
+
+GEMM_API gemm_status_t gemm_last_device_status(cudaStream_t stream) {
+    int status = 0;
+    if (gemm::tc_read_and_clear_status(stream, &status) != cudaSuccess) return GEMM_ERR_INTERNAL;
+    return status ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }

@@ -1,0 +1,602 @@
+// gemm_tc.cu -- BF16-input, FP32-accumulate GEMM on the sm_103a tensor cores.
+//
+// D = alpha * op(A) * op(B) + beta * C, D row-major FP32.
+//
+// Design (what the pages prescribe, rebuilt for tcgen05):
+//   * Accumulators live in tensor memory (TMEM); A and B are read by the
+//     tensor core straight from shared memory through matrix descriptors
+//     ("GEMM on NVIDIA GPUs", section 4, "Tensor Core pipeline": on
+//     Blackwell tcgen05.mma keeps the accumulator in TMEM and takes B from
+//     shared memory).
+//   * TMA fills a STAGES-deep ring of 128-byte-swizzled A/B tiles; full/empty
+//     mbarriers hand each stage from the load warp to the MMA warp and back
+//     ("Worklog: optimising GEMM on NVIDIA H100", kernel 7 TMA + barriers,
+//     and the producer/consumer pipeline after kernel 8).
+//   * Warp roles: warp 0 issues TMA (one lane), warp 1 owns TMEM and issues
+//     tcgen05.mma (one lane), warps 2-5 run the epilogue.
+//   * Persistent grid (one CTA per SM), static round-robin over output tiles
+//     in grouped order along M so that CTAs running together share A and B
+//     panels in L2 ("GEMM on NVIDIA GPUs", section 5 / grouped schedulers).
+//   * Two TMEM accumulators (2 x 256 columns): the epilogue of tile i runs
+//     while the MMA warp accumulates tile i + 1.
+//   * Epilogue: tcgen05.ld TMEM -> registers, D = alpha * acc + beta * C
+//     (C read only when beta != 0), guarded stores; tiles past the matrix
+//     edge are zero-filled by TMA on the way in and clipped on the way out.
+//   * Every barrier wait is bounded; a wait that runs out records a timeout
+//     in a device status word, the CTA drains what it has in flight, frees
+//     TMEM and exits.
+//
+// Tile: BM x BN x BK = 128 x 256 x 64; one tcgen05.mma is 128 x 256 x 16,
+// four per K block.  A stage holds 16 KiB of A and 32 KiB of B.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace gemm {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 BF16 = 128 bytes = one swizzle row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
+constexpr int NUM_THREADS = 192;          // 6 warps
+constexpr int kGroupM = 8;
+// ring + barriers + slack for aligning the ring to 1024 bytes
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+__device__ int g_tc_status;  // 0 = fine, 1 = a bounded wait ran out
+
+struct TcArgs {
+    int64_t M, N, K;
+    float alpha, beta;
+    const float *C;
+    int64_t ldc;
+    float *D;
+    int64_t ldd;
+    int64_t tiles_m, tiles_n, num_kb;
+    int a_kmajor, b_kmajor;
+    int vec_c, vec_d;
+    uint64_t timeout_ns;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Gives up
+// (returns false) when the CTA's abort flag is raised or after timeout_ns.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             const volatile int *abort_flag,
+                                             uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_timer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer() - start > timeout_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void raise_abort(volatile int *abort_flag) {
+    *abort_flag = 1;
+    atomicExch(&g_tc_status, 1);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0,
+                                            int32_t c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM words: thread t of the warp gets its
+// lane's 32 consecutive columns.
+__device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------- matrix descriptors
+// tcgen05 shared-memory matrix descriptor (64 bits):
+//   [0,14)  start address >> 4        [16,30) leading-dimension byte offset >> 4
+//   [32,46) stride-dimension byte offset >> 4
+//   [46,48) version = 1               [49,52) base offset (0: atoms 1024-aligned)
+//   [52]    LBO mode = 0              [61,64) swizzle: 2 = 128-byte swizzle
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// K-major operand: rows of 64 BF16 (128 B), 8-row swizzle atoms of 1 KiB
+// stacked along M/N (SBO = 1024).  The k-th 16-wide slice starts 32 B in.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+    return smem_desc(tile + kk * UMMA_K * 2, 16, 1024);
+}
+
+// MN-major operand: per 64-element MN block, 64 K-rows of 128 B (8 KiB);
+// blocks stacked along MN (LBO = 8 KiB), 8-row groups along K (SBO = 1 KiB).
+// The k-th 16-deep slice starts 16 rows = 2 KiB in.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+    return smem_desc(tile + kk * UMMA_K * 128, 64 * 128, 1024);
+}
+
+// Instruction descriptor, kind::f16: D FP32 (bits 4-5 = 1), A and B BF16
+// (bits 7-9 = 1, 10-12 = 1), A/B major-ness (bit 15 / 16: 0 = K-major,
+// 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t &tm,
+                                            int64_t &tn) {
+    const int64_t width = kGroupM * a.tiles_n;
+    const int64_t first_m = (t / width) * kGroupM;
+    const int64_t rest = a.tiles_m - first_m;
+    const int64_t gsz = rest < kGroupM ? rest : kGroupM;
+    tm = first_m + (t % width) % gsz;
+    tn = (t % width) / gsz;
+}
+
+// D[row, c0 .. c0+31] = alpha * acc + beta * C[row, ...] for one thread's row,
+// with 16-byte accesses where the row allows and per-element guards at the edge.
+__device__ __forceinline__ void store_row_chunk(const TcArgs &args, const uint32_t (&v)[32],
+                                                float *drow, const float *crow, int64_t c0,
+                                                bool use_c) {
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const int64_t col = c0 + j4 * 4;
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = args.alpha * __uint_as_float(v[j4 * 4 + j]);
+        const bool full4 = col + 3 < args.N;
+        if (use_c) {
+            if (full4 && args.vec_c) {
+                // plain load: C may be D itself (in-place update)
+                const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+                o[0] = fmaf(args.beta, c.x, o[0]);
+                o[1] = fmaf(args.beta, c.y, o[1]);
+                o[2] = fmaf(args.beta, c.z, o[2]);
+                o[3] = fmaf(args.beta, c.w, o[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < args.N) o[j] = fmaf(args.beta, crow[col + j], o[j]);
+            }
+        }
+        if (full4 && args.vec_d) {
+            *reinterpret_cast<float4 *>(drow + col) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (col + j < args.N) drow[col + j] = o[j];
+        }
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b, const TcArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    // the ring must be 1024-byte aligned for the 128-byte swizzle atoms
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *full = bars;                  // [STAGES]  TMA -> MMA
+    uint64_t *empty = bars + STAGES;        // [STAGES]  MMA -> TMA
+    uint64_t *tfull = bars + 2 * STAGES;    // [2]       MMA -> epilogue
+    uint64_t *tempty = tfull + ACC_BUFS;    // [2]       epilogue -> MMA
+    uint64_t *drain = tempty + ACC_BUFS;    // [1]       MMA teardown
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            mbar_init(smem_addr(&tfull[b]), 1);
+            mbar_init(smem_addr(&tempty[b]), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(smem_addr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b))
+                     : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t n_tiles = args.tiles_m * args.tiles_n;
+    const uint32_t ring_base = smem_addr(ring);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                int64_t tm, tn;
+                tile_coords(t, args, tm, tn);
+                const int32_t m0 = static_cast<int32_t>(tm * BM);
+                const int32_t n0 = static_cast<int32_t>(tn * BN);
+                for (int64_t kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
+                                      args.timeout_ns)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    const uint32_t sa = ring_base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const int32_t k0 = static_cast<int32_t>(kb * BK);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (args.a_kmajor) {
+                        tma_load_2d(sa, &map_a, k0, m0, fb);
+                    } else {
+                        for (int i = 0; i < BM / 64; ++i)
+                            tma_load_2d(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
+                    }
+                    if (args.b_kmajor) {
+                        tma_load_2d(sb, &map_b, k0, n0, fb);
+                    } else {
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_2d(sb + i * 64 * 128, &map_b, n0 + 64 * i, k0, fb);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // Let the copies still in flight land before the CTA can exit:
+            // wait on the full barrier of each of the last issued stages.
+            const int64_t outstanding = issued < STAGES ? issued : STAGES;
+            int s = stage;
+            uint32_t ph = phase;
+            for (int64_t i = 0; i < outstanding; ++i) {
+                if (--s < 0) {
+                    s = STAGES - 1;
+                    ph ^= 1;
+                }
+                // bounded, and independent of the abort flag: the copies were issued
+                const volatile int never = 0;
+                if (!wait_bounded(smem_addr(&full[s]), ph, &never, args.timeout_ns))
+                    raise_abort(abort_flag);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(!args.a_kmajor, !args.b_kmajor);
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t li = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++li) {
+                const int buf = static_cast<int>(li & 1);
+                const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
+                if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
+                                  args.timeout_ns)) {
+                    raise_abort(abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int64_t kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag,
+                                      args.timeout_ns)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = ring_base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = args.a_kmajor ? desc_kmajor(sa, kk) : desc_mnmajor(sa, kk);
+                        const uint64_t bd = args.b_kmajor ? desc_kmajor(sb, kk) : desc_mnmajor(sb, kk);
+                        tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_addr(&empty[stage]));  // frees the stage when these MMAs finish
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(smem_addr(&tfull[buf]));  // accumulator ready for the epilogue
+            }
+            // all MMAs this thread issued have finished once `drain` completes
+            tc_commit(smem_addr(drain));
+            const volatile int never = 0;
+            if (!wait_bounded(smem_addr(drain), 0, &never, args.timeout_ns))
+                raise_abort(abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- epilogue warps 2-5
+        const int quarter = warp % 4;  // TMEM lanes this warp may access
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool use_c = args.beta != 0.f;
+        int64_t li = 0;
+        for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++li) {
+            const int buf = static_cast<int>(li & 1);
+            const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
+            // lane 0 waits, the warp follows its verdict (keeps the warp converged)
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_addr(&tfull[buf]), acc_phase, abort_flag, args.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_abort(abort_flag);
+                break;
+            }
+            tc_fence_after();
+            int64_t tm, tn;
+            tile_coords(t, args, tm, tn);
+            const int64_t row = tm * BM + quarter * 32 + lane;
+            const bool row_ok = row < args.M;
+            float *drow = args.D + row * args.ldd;
+            const float *crow = use_c ? args.C + row * args.ldc : nullptr;
+            const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                uint32_t v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective: converge first
+                tmem_load_32cols(t_acc + chunk * 32, v);
+                if (chunk == BN / 32 - 1) {
+                    // accumulator buffer fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&tempty[buf]));
+                }
+                const int64_t c0 = tn * BN + chunk * 32;
+                if (row_ok && c0 < args.N) store_row_chunk(args, v, drow, crow, c0, use_c);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D BF16 tensor map: inner dimension `inner` (contiguous), outer `outer`,
+// row pitch ld elements, box = box_inner x box_outer, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int64_t ld,
+               uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attr_done[kMaxDevices];
+
+int device_sm_count(int dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    return n > 0 ? n : 1;
+}
+
+bool aligned(const void *ptr, size_t bytes) {
+    return (reinterpret_cast<uintptr_t>(ptr) % bytes) == 0;
+}
+
+}  // namespace
+
+bool tc_eligible(const Problem &p) {
+    // TMA: global base 16-byte aligned, row pitch a multiple of 16 bytes,
+    // extents below 2^31 (coordinates are signed 32-bit).
+    return aligned(p.A, 16) && aligned(p.B, 16) && (p.lda % 8 == 0) && (p.ldb % 8 == 0) &&
+           p.M < (int64_t(1) << 31) && p.N < (int64_t(1) << 31) && p.K < (int64_t(1) << 31);
+}
+
+cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) {
+    if (!tc_eligible(p)) return cudaErrorNotSupported;
+    if (!load_encoder()) return cudaErrorSymbolNotFound;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices && !g_attr_done[dev].load()) {
+        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        g_attr_done[dev].store(1);
+    } else if (dev >= kMaxDevices) {
+        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+    }
+
+    CUtensorMap map_a, map_b;
+    bool ok;
+    if (p.a_kmajor)  // A(i, k) at A[i * lda + k]: inner K, outer M
+        ok = encode_2d(&map_a, p.A, p.K, p.M, p.lda, BK, BM);
+    else  // A(i, k) at A[i + k * lda]: inner M, outer K
+        ok = encode_2d(&map_a, p.A, p.M, p.K, p.lda, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+    if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N
+        ok = encode_2d(&map_b, p.B, p.K, p.N, p.ldb, BK, BN);
+    else  // B(k, j) at B[k * ldb + j]: inner N, outer K
+        ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+
+    TcArgs a;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.D = p.D;
+    a.ldd = p.ldd;
+    a.tiles_m = (p.M + BM - 1) / BM;
+    a.tiles_n = (p.N + BN - 1) / BN;
+    a.num_kb = (p.K + BK - 1) / BK;
+    a.a_kmajor = p.a_kmajor ? 1 : 0;
+    a.b_kmajor = p.b_kmajor ? 1 : 0;
+    a.vec_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
+    a.vec_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
+    a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+
+    const int64_t tiles = a.tiles_m * a.tiles_n;
+    const int64_t sms = device_sm_count(dev);
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_a, map_b, a);
+    *name = "gemm_bf16_tc";
+    return cudaGetLastError();
+}
+
+cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(status, g_tc_status, sizeof(int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                    stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    return e;
+}
+
+}  // namespace gemm

@@ -1,0 +1,42 @@
+// internal.h -- what the host dispatcher and the kernel launchers share.
+//
+// After normalisation every kernel sees D as row-major M x N; op(A) and op(B)
+// keep their own storage order, described by whether K is the contiguous
+// ("K-major") dimension.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gemm {
+
+struct Problem {
+    int64_t M, N, K;
+    float alpha, beta;
+    const void *A;
+    int64_t lda;
+    bool a_kmajor;  // A(i, k) at A[i * lda + k]; else A[i + k * lda]
+    const void *B;
+    int64_t ldb;
+    bool b_kmajor;  // B(k, j) at B[k + j * ldb]; else B[k * ldb + j]
+    const float *C;  // read only if beta != 0; row-major, ldc
+    int64_t ldc;
+    float *D;  // row-major, ldd
+    int64_t ldd;
+};
+
+enum class InType { F32, BF16 };
+
+// Each launcher enqueues one kernel on `stream`, returns the CUDA error of
+// the launch and sets *name to the kernel's static name.
+cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name);
+cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **name);
+
+// Tensor-core (tcgen05) path for BF16 inputs.  Returns cudaErrorNotSupported
+// (without launching) when the operands cannot be described by TMA.
+bool tc_eligible(const Problem &p);
+cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name);
+// Reads and clears the tensor-core kernel's device status word (after a sync).
+cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status);
+
+}  // namespace gemm

@@ -1,0 +1,153 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Both entry points compute, on the GPU,
+ *
+ *     D = alpha * op(A) * op(B) + beta * C
+ *
+ * the general matrix multiplication of "GEMM on NVIDIA GPUs: from naive
+ * kernel to tiled pipeline", section 1 "GEMM definition": op(A) is M x K,
+ * op(B) is K x N, C and D are M x N, and
+ *
+ *     D_ij = alpha * sum_{k<K} A_ik * B_kj + beta * C_ij.
+ *
+ * "op" (identity or transpose) is expressed as the storage order of each
+ * operand, which is exactly the BLAS "trans" flag:
+ *
+ *     GEMM_ROW_MAJOR:  X(r, q) is stored at X[r * ld + q]
+ *     GEMM_COL_MAJOR:  X(r, q) is stored at X[r + q * ld]
+ *
+ * where (r, q) index the LOGICAL matrix: A(i, k), B(k, j), C(i, j), D(i, j).
+ * C and D share one order.  Leading dimensions are in elements.
+ *
+ * Common contract of gemm_f32 and gemm_bf16_f32acc
+ * -------------------------------------------------
+ * Ownership: A, B, C and D are device pointers owned by the caller (for
+ *   example torch CUDA tensors).  The library keeps no pointer after the call
+ *   returns and allocates no device memory on these paths; tensor maps travel
+ *   by value in the launch parameters.  The library holds no per-call state
+ *   and may be called from several host threads.
+ * Asynchrony: the work is enqueued on `stream` (0 = the legacy default
+ *   stream) and the call returns without waiting for it.  The caller keeps
+ *   the buffers alive until the stream has passed the call.
+ * Shapes: M, N, K >= 0 and each <= 2^31 - 1.  M == 0 or N == 0 is a no-op
+ *   that returns GEMM_OK without touching any pointer.  K == 0 or
+ *   alpha == 0 gives D = beta * C (A and B are not read).
+ * beta == 0: C is never read and may be NULL (BLAS convention; C traffic
+ *   only counts when beta != 0 in "GEMM on NVIDIA GPUs", section 2, "GEMM
+ *   arithmetic intensity").  C == D with the same ldc/ldd is allowed
+ *   (in-place update).  Any other overlap of D with A, B or C is undefined.
+ * Leading dimensions: lda >= max(1, K) if A is row-major, >= max(1, M) if
+ *   column-major; ldb >= max(1, N) row-major / max(1, K) column-major;
+ *   ldc, ldd >= max(1, N) row-major / max(1, M) column-major.
+ * Alignment: pointers must be aligned to their element size.  Any leading
+ *   dimension is accepted; wide loads and TMA are used when pointers and
+ *   leading dimensions allow it, narrower guarded accesses otherwise.  This
+ *   never changes the result beyond the stated tolerances and is never an
+ *   error.
+ * Edges: any M, N, K is handled; tiles past the matrix edge read zeros and
+ *   never store outside D.
+ * Errors: argument errors return synchronously before any launch and leave
+ *   D untouched.  A launch failure returns GEMM_ERR_LAUNCH.  A device without
+ *   sm_103 support returns GEMM_ERR_UNSUPPORTED_DEVICE (no CPU fallback
+ *   exists).  The tensor-core kernel bounds every wait on its pipeline
+ *   barriers; if one runs out it records GEMM_ERR_TIMEOUT in a per-device
+ *   status word, read by gemm_last_device_status().  Nothing is printed.
+ */
+#ifndef DENSE_GEMM_08_GB300_GEMM_H
+#define DENSE_GEMM_08_GB300_GEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,     /* bad shape, leading dimension, order, NULL or misaligned pointer */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 */
+    GEMM_ERR_LAUNCH = 3,            /* the CUDA runtime refused the launch */
+    GEMM_ERR_TIMEOUT = 4,           /* a bounded device-side wait ran out (see gemm_last_device_status) */
+    GEMM_ERR_INTERNAL = 5           /* a CUDA runtime or driver call failed (e.g. tensor-map encoding) */
+} gemm_status_t;
+
+/* One BF16 number as its raw 16-bit pattern (the upper half of an FP32). */
+typedef uint16_t gemm_bf16_t;
+
+/*
+ * gemm_f32 -- FP32 inputs, FP32 arithmetic on the CUDA cores (no TF32),
+ * FP32 output.  The kernel tiles D into CTA tiles staged through shared
+ * memory, each thread accumulates an 8 x 8 register block with FP32 FMA
+ * ("Worklog: optimising GEMM on NVIDIA H100", kernels 2-6: shared-memory
+ * tiling, register tiling, vectorised loads, warp tiling).
+ *
+ *   M, N, K        logical sizes of op(A) (M x K), op(B) (K x N), C/D (M x N)
+ *   alpha, beta    scalars (FP32)
+ *   A, lda, order_a   device pointer to op(A)'s storage, its leading dimension, its order
+ *   B, ldb, order_b   same for op(B)
+ *   C, ldc         device pointer to C (read only if beta != 0), leading dimension
+ *   D, ldd         device pointer to D (written), leading dimension
+ *   order_cd       storage order of both C and D
+ *   stream         CUDA stream the kernel is enqueued on
+ *
+ * Accuracy: |D - D_ref| <= 1e-5 * sum_k |alpha A_ik B_kj| + 1e-6 * |beta C_ij|
+ * against the exact result; bit-exact when every partial sum is an integer
+ * below 2^24 and alpha = 1, beta = 0.
+ */
+gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
+                       const float *A, int64_t lda, gemm_order_t order_a,
+                       const float *B, int64_t ldb, gemm_order_t order_b,
+                       float beta, const float *C, int64_t ldc,
+                       float *D, int64_t ldd, gemm_order_t order_cd,
+                       cudaStream_t stream);
+
+/*
+ * gemm_bf16_f32acc -- BF16 inputs, FP32 accumulation, FP32 C and D.
+ *
+ * The tensor-core path (tcgen05.mma with the accumulator in tensor memory,
+ * "GEMM on NVIDIA GPUs", section 4 "Tensor Core pipeline"; TMA-fed
+ * multi-stage shared-memory ring with a producer/consumer split,
+ * "Worklog: optimising GEMM on NVIDIA H100", kernels 7-9) runs when A and B
+ * are 16-byte aligned and lda, ldb are multiples of 8 elements.  Otherwise a
+ * CUDA-core kernel with the same results contract runs.  Arguments as for
+ * gemm_f32; A and B point to BF16 bit patterns.
+ *
+ * Accuracy: |D - D_ref| <= 4e-3 * sum_k |alpha A_ik B_kj| + 1e-6 against the
+ * exact result over the same BF16 inputs; bit-exact when every partial sum
+ * is an integer below 2^24 and alpha = 1, beta = 0.
+ */
+gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
+                               const gemm_bf16_t *A, int64_t lda, gemm_order_t order_a,
+                               const gemm_bf16_t *B, int64_t ldb, gemm_order_t order_b,
+                               float beta, const float *C, int64_t ldc,
+                               float *D, int64_t ldd, gemm_order_t order_cd,
+                               cudaStream_t stream);
+
+/* Static English description of a status code; never NULL. */
+const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * gemm_last_device_status -- synchronises `stream`, then reads and clears
+ * the current device's status word.  Returns GEMM_OK, or GEMM_ERR_TIMEOUT if
+ * a tensor-core launch on this device gave up a bounded wait since the last
+ * read (its D is then incomplete), or GEMM_ERR_INTERNAL if the read itself
+ * failed.
+ */
+gemm_status_t gemm_last_device_status(cudaStream_t stream);
+
+/*
+ * gemm_last_kernel -- name of the kernel the calling host thread's most
+ * recent successful gemm_* call enqueued ("" if it enqueued none, e.g. for
+ * M == 0).  Static string; for tests and launch accounting.
+ */
+const char *gemm_last_kernel(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_08_GB300_GEMM_H */

@@ -1,0 +1,75 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports exactly
+the entry points include/gemm.h declares, and rejects bad arguments before
+touching CUDA (argument checks need no device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_gemm_08_gb300 as lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    dll = lib.library()
+    for name in declared_functions():
+        assert hasattr(dll, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines()
+                      if " T " in line and not line.split()[-1].startswith("_"))
+    assert exported == declared_functions()
+
+
+def test_status_strings():
+    for st in range(6):
+        assert lib.gemm_status_string(st)
+    assert lib.gemm_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("fn_name", ["gemm_f32", "gemm_bf16_f32acc"])
+def test_argument_errors_without_a_device(fn_name):
+    fn = getattr(lib, fn_name)
+    fake = 1 << 20  # never dereferenced: the checks run before any CUDA call
+    good = dict(M=8, N=8, K=8, alpha=1.0, A=fake, lda=8, oa=0, B=fake, ldb=8, ob=0, beta=0.0,
+                C=None, ldc=8, D=fake, ldd=8, ocd=0)
+    bad = [dict(M=-1), dict(N=-3), dict(K=-1), dict(M=1 << 31), dict(oa=2), dict(ocd=5),
+           dict(lda=7), dict(ldb=7), dict(ldd=7), dict(oa=1, lda=7), dict(ocd=1, ldd=7),
+           dict(beta=1.0), dict(beta=1.0, C=fake, ldc=7), dict(A=None), dict(B=None),
+           dict(D=None), dict(D=fake + 2), dict(A=fake + 1), dict(C=fake + 2, beta=1.0)]
+    for change in bad:
+        a = dict(good, **change)
+        st = fn(a["M"], a["N"], a["K"], a["alpha"], a["A"], a["lda"], a["oa"], a["B"], a["ldb"],
+                a["ob"], a["beta"], a["C"], a["ldc"], a["D"], a["ldd"], a["ocd"], stream=0,
+                check=False)
+        assert st == lib.GEMM_ERR_INVALID_VALUE, change
+    # M == 0 is a no-op even with NULL pointers
+    assert fn(0, 8, 8, 1.0, None, 8, 0, None, 8, 0, 0.0, None, 8, None, 8, 0, stream=0) == 0
+    assert lib.gemm_last_kernel() == ""
+
+
+def test_valid_call_without_a_device_reports_unsupported_device():
+    # all arguments valid: the library then needs an sm_103 device and says so
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fake = 1 << 20
+    st = lib.gemm_f32(8, 8, 8, 1.0, fake, 8, 0, fake, 8, 0, 0.0, None, 8, fake, 8, 0, stream=0,
+                      check=False)
+    assert st == lib.GEMM_ERR_UNSUPPORTED_DEVICE

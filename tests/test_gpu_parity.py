@@ -1,0 +1,249 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Every test calls the C ABI (through the package binding) on seeded inputs
+and compares with the oracle on the same bits:
+  * FP32:  |D - D_ref| <= 1e-5 * sum_k|alpha A_ik B_kj| + 1e-6 * |beta C_ij|
+  * BF16:  |D - D_ref| <= 4e-3 * sum_k|alpha A_ik B_kj| + 1e-6
+  * small-integer inputs (every partial sum exact in FP32): bit-exact.
+Full-size workloads are checked on sampled entries (whole rows and columns,
+tile-boundary entries, corners, random entries) that the oracle computes one
+by one; moderate sizes spanning several tiles with ragged tails are checked
+in full, together with a guard band around D.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_08_gb300 as lib
+from dense_gemm_08_gb300.inputs import COL, ROW, WORKLOADS, Workload, make_inputs
+from gemm_harness import (assert_within, c_logical, check_canary, logical_d, oracle_full,
+                          oracle_points, run_gpu, sample_points)
+
+pytestmark = pytest.mark.gpu
+
+ORDERS = list(itertools.product((ROW, COL), repeat=3))
+
+
+def full_check(w, inp, pad_d=0, expect_kernel=None):
+    Dbuf, ldd, name = run_gpu(w, inp, pad_d=pad_d)
+    if expect_kernel is not None:
+        assert name.startswith(expect_kernel), name
+    D = logical_d(w, Dbuf)
+    ref, S = oracle_full(w, inp)
+    ratio = assert_within(w, D, ref, S, c_logical(w, inp))
+    if pad_d:
+        check_canary(w, Dbuf)
+    return D, ref, ratio
+
+
+def sampled_check(w, inp, rows, cols, n_random=4000, seed=0):
+    Dbuf, ldd, name = run_gpu(w, inp)
+    D = logical_d(w, Dbuf)
+    rng = np.random.default_rng(seed)
+    I, J = sample_points(w.M, w.N, rng, n_random, rows, cols)
+    ref, S = oracle_points(w, inp, I, J)
+    C = c_logical(w, inp)
+    Cv = C[I, J] if C is not None else None
+    assert np.isfinite(D).all(), f"{w.name}: non-finite output"
+    return assert_within(w, D[I, J], ref, S, Cv, "sampled"), name
+
+
+# ---------------------------------------------------------------- the configs
+def test_f32_256_full():
+    w = WORKLOADS["f32_256"]
+    full_check(w, make_inputs(w), pad_d=3, expect_kernel="sgemm_simt<f32")
+
+
+def test_f32_256_small_integers_bit_exact():
+    w = WORKLOADS["f32_256_int"]
+    inp = make_inputs(w)
+    Dbuf, _, _ = run_gpu(w, inp)
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("name", ["f32_4096", "bf16_8192", "bf16_mlp"])
+def test_full_size_config_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    ratio, kernel = sampled_check(w, inp, rows=(0, 1, w.M // 2 + 3, w.M - 1),
+                                  cols=(0, w.N // 3 + 1, w.N - 1))
+    if w.dtype == "bf16":
+        assert kernel == "gemm_bf16_tc"
+
+
+@pytest.mark.parametrize("name", sorted(k for k in WORKLOADS if k.startswith("odd_")))
+def test_odd_shape_sweep(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    if w.M * w.N * w.K <= 64 * 1024 * 1024:
+        full_check(w, inp)
+    else:
+        sampled_check(w, inp, rows=(0, w.M // 2, w.M - 1), cols=(0, w.N - 1), n_random=3000)
+
+
+# ------------------------------------------- moderate sizes, checked in full
+MODERATE = (300, 600, 200)  # 3 x 3 tensor-core tiles with ragged M, N and K tails
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_orders_full(dtype, orders):
+    M, N, K = MODERATE
+    w = Workload(f"mod_{dtype}", M, N, K, 1.5, -0.25, dtype, *orders)
+    inp = make_inputs(w, seed=1, pad=3, ld_multiple=8)
+    expect = "gemm_bf16_tc" if dtype == "bf16" else "sgemm_simt<f32"
+    full_check(w, inp, pad_d=5, expect_kernel=expect)
+
+
+@pytest.mark.parametrize("shape", [(257, 515, 1000), (128, 256, 64), (1, 1, 1), (129, 1, 77),
+                                   (1, 300, 513), (640, 512, 8)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_integers_bit_exact(dtype, shape):
+    M, N, K = shape
+    for orders in [(ROW, COL, ROW), (COL, ROW, ROW), (ROW, ROW, COL)]:
+        w = Workload("int", M, N, K, 1.0, 0.0, dtype, *orders, dist="int")
+        inp = make_inputs(w, seed=2, ld_multiple=8)
+        Dbuf, _, _ = run_gpu(w, inp)
+        ref, _ = oracle_full(w, inp)
+        assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32)), orders
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_shapes_brute_force(dtype):
+    """Every (M, N, K) in {1..5}^3, every storage order, two (alpha, beta)."""
+    for M, N, K in itertools.product(range(1, 6), repeat=3):
+        for orders in ORDERS:
+            for alpha, beta in ((1.0, 0.0), (1.5, -0.25)):
+                w = Workload("tiny", M, N, K, alpha, beta, dtype, *orders, dist="int")
+                # ld a multiple of 8 keeps BF16 on the tensor-core path
+                inp = make_inputs(w, seed=M * 100 + N * 10 + K, ld_multiple=8)
+                Dbuf, _, name = run_gpu(w, inp)
+                ref, _ = oracle_full(w, inp)
+                got = logical_d(w, Dbuf)
+                assert np.array_equal(got, ref.astype(np.float32)), (M, N, K, orders, alpha,
+                                                                    beta, name)
+
+
+# ------------------------------------------------------------- edge cases
+def _dev(t):
+    return t.to("cuda") if t is not None else None
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_empty_shapes_are_noops(dtype):
+    fn = lib.gemm_f32 if dtype == "f32" else lib.gemm_bf16_f32acc
+    D = torch.full((4, 4), 7.0, device="cuda")
+    assert fn(0, 4, 4, 1.0, None, 4, ROW, None, 4, ROW, 0.0, None, 4, D, 4, ROW) == 0
+    assert fn(4, 0, 4, 1.0, None, 4, ROW, None, 4, ROW, 0.0, None, 4, D, 4, ROW) == 0
+    assert lib.gemm_last_kernel() == ""
+    torch.cuda.synchronize()
+    assert torch.all(D == 7.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_k_zero_and_alpha_zero_give_beta_c(dtype):
+    w = Workload("kz", 70, 90, 0, 1.5, -0.25, dtype)
+    inp = make_inputs(w, seed=3)
+    full_check(w, inp, pad_d=2, expect_kernel="scale_c")
+    # alpha = 0: A and B are not read (they hold NaN here)
+    w = Workload("a0", 70, 90, 33, 0.0, 2.0, dtype)
+    inp = make_inputs(w, seed=3)
+    inp["A"] = torch.full_like(inp["A"], float("nan"))
+    Dbuf, _, name = run_gpu(w, inp)
+    assert name == "scale_c"
+    assert np.array_equal(logical_d(w, Dbuf), (2.0 * inp["C_logical"]).numpy())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_beta_zero_never_reads_c(dtype):
+    w = Workload("b0", 200, 300, 64, 1.0, 0.0, dtype, ROW, COL, ROW)
+    inp = make_inputs(w, seed=4, ld_multiple=8)
+    A, B = _dev(inp["A"]), _dev(inp["B"])
+    Cnan = torch.full((w.M, w.N), float("nan"), device="cuda")
+    D = torch.empty((w.M, w.N), device="cuda")
+    fn = lib.gemm_f32 if dtype == "f32" else lib.gemm_bf16_f32acc
+    fn(w.M, w.N, w.K, 1.0, A, inp["lda"], ROW, B, inp["ldb"], COL, 0.0, Cnan, w.N, D, w.N, ROW)
+    torch.cuda.synchronize()
+    assert torch.isfinite(D).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_in_place_c_equals_d(dtype):
+    w = Workload("inplace", 260, 520, 130, 0.5, 1.0, dtype, ROW, COL, ROW)
+    inp = make_inputs(w, seed=5, ld_multiple=8)
+    Dbuf, _, _ = run_gpu(w, inp, in_place=True)
+    ref, S = oracle_full(w, inp)
+    assert_within(w, logical_d(w, Dbuf), ref, S, c_logical(w, inp))
+
+
+def test_bf16_unaligned_operands_use_cuda_core_path():
+    """lda not a multiple of 8, and an operand starting 2 bytes off a 16-byte boundary."""
+    w = Workload("unal", 150, 270, 101, 1.5, -0.25, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=6)  # lda = ldb = 101
+    full_check(w, inp, pad_d=1, expect_kernel="sgemm_simt<bf16")
+    # shift B by one element inside a bigger buffer
+    inp2 = make_inputs(w, seed=6, ld_multiple=8)
+    Bbig = torch.zeros(inp2["B"].numel() + 8, dtype=torch.bfloat16)
+    Bbig[1:1 + inp2["B"].numel()] = inp2["B"].reshape(-1)
+    A, Bd = _dev(inp2["A"]), Bbig.to("cuda")
+    C = _dev(inp2["C"])
+    D = torch.empty((w.M, w.N), device="cuda")
+    lib.gemm_bf16_f32acc(w.M, w.N, w.K, w.alpha, A, inp2["lda"], ROW, Bd.data_ptr() + 2,
+                         inp2["ldb"], COL, w.beta, C, inp2["ldc"], D, w.N, ROW)
+    assert lib.gemm_last_kernel().startswith("sgemm_simt<bf16")
+    torch.cuda.synchronize()
+    ref, S = oracle_full(w, inp2)
+    assert_within(w, D.cpu().numpy(), ref, S, c_logical(w, inp2))
+
+
+def test_f32_unaligned_leading_dimensions():
+    """Leading dimensions that are not multiples of 4 (scalar loads and stores)."""
+    for orders in [(ROW, ROW, ROW), (COL, COL, COL)]:
+        w = Workload("f32lds", 333, 257, 129, 1.5, -0.25, "f32", *orders)
+        inp = make_inputs(w, seed=7, pad=1)
+        full_check(w, inp, pad_d=1)
+
+
+def test_invalid_arguments_are_rejected_before_launch():
+    D = torch.zeros((8, 8), device="cuda")
+    A = torch.zeros((8, 8), device="cuda")
+    bad = [
+        dict(M=-1),
+        dict(lda=7),                    # row-major A needs lda >= K
+        dict(ldd=7),                    # row-major D needs ldd >= N
+        dict(order_a=2),
+        dict(beta=1.0, C=None),         # beta != 0 needs C
+        dict(A=None),
+        dict(D=None),
+        dict(A=A.data_ptr() + 2),       # misaligned FP32 pointer
+    ]
+    for change in bad:
+        args = dict(M=8, N=8, K=8, alpha=1.0, A=A, lda=8, order_a=ROW, B=A, ldb=8, order_b=ROW,
+                    beta=0.0, C=None, ldc=8, D=D, ldd=8, order_cd=ROW)
+        args.update(change)
+        st = lib.gemm_f32(args["M"], args["N"], args["K"], args["alpha"], args["A"],
+                          args["lda"], args["order_a"], args["B"], args["ldb"], args["order_b"],
+                          args["beta"], args["C"], args["ldc"], args["D"], args["ldd"],
+                          args["order_cd"], check=False)
+        assert st == lib.GEMM_ERR_INVALID_VALUE, change
+
+
+def test_device_status_is_clean_after_runs():
+    w = WORKLOADS["bf16_8192"].with_(M=1000, N=1000, K=1000)
+    inp = make_inputs(w)
+    run_gpu(w, inp)
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+
+
+def test_torch_helper_matches_oracle():
+    w = Workload("helper", 300, 260, 90, 1.0, 0.0, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=8, ld_multiple=8)
+    A = inp["A_logical"].to("cuda")
+    Bt = inp["B_logical"].t().contiguous().to("cuda")  # N x K storage: B column-major
+    D = lib.gemm(A, Bt.t())
+    torch.cuda.synchronize()
+    ref, S = oracle_full(w, inp)
+    assert_within(w, D.cpu().numpy(), ref, S, None)
