@@ -109,7 +109,7 @@ def clock_summary(rows):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -123,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -223,10 +223,19 @@ def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None):
                       f"{dt:.2f} s", "seconds": dt, "_rows": rows, "_D": D, "_S": S}
 
 
+def resolve_workload(args):
+    from dense_gemm_08_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.split(","))
+        w = w.with_(name=f"{w.name}@{M}x{N}x{K}", M=M, N=N, K=K)
+    return w
+
+
 def bench_ours(args):
     import torch
     import dense_gemm_08_gb300 as lib
-    from dense_gemm_08_gb300.inputs import WORKLOADS, make_inputs
+    from dense_gemm_08_gb300.inputs import make_inputs
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -234,7 +243,7 @@ def bench_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    w = WORKLOADS[args.workload]
+    w = resolve_workload(args)
     inp = make_inputs(w, seed=0)
     fn = lib.gemm_f32 if w.dtype == "f32" else lib.gemm_bf16_f32acc
     in_bytes = 4 if w.dtype == "f32" else 2
@@ -404,11 +413,11 @@ def bench_ours(args):
 
 # ---------------------------------------------------------- reference arm
 def bench_reference(args):
-    from dense_gemm_08_gb300.inputs import WORKLOADS, make_inputs
+    from dense_gemm_08_gb300.inputs import make_inputs
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    w = WORKLOADS[args.workload]
+    w = resolve_workload(args)
     inp = make_inputs(w, seed=0)
     per_step = max(0.5, min(10.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -439,9 +448,11 @@ def bench_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="bf16_8192")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K overriding the workload's sizes (profiling on smaller cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

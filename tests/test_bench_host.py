@@ -1,0 +1,100 @@
+"""bench.py host logic on the CPU: byte/FLOP model, roofline, peaks, clock
+parsing, the committed-traffic lookup and the max-over-ranks timing with two
+gloo ranks."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from dense_gemm_08_gb300.inputs import WORKLOADS
+from golden.fixtures import read as read_fixture
+
+
+def test_algorithmic_bytes_match_the_pages_and_the_configs():
+    g = read_fixture("p5_4096_fp32_traffic.txt")
+    # FP32 n^3, inputs read once, output written once: 12 n^2 bytes
+    assert bench.algorithmic_bytes(4096, 4096, 4096, 4, 0.0) == int(g["Q_one_pass"])
+    assert bench.algorithmic_bytes(8192, 8192, 8192, 2, 0.0) == 536_870_912
+    mlp = WORKLOADS["bf16_mlp"]
+    assert bench.algorithmic_bytes(mlp.M, mlp.N, mlp.K, 2, mlp.beta) == 1_124_073_472
+    assert bench.algorithmic_bytes(4095, 4097, 1000, 4, -0.25) == 166_985_720
+    assert bench.algorithmic_bytes(4095, 4097, 1000, 2, -0.25) == 150_601_720
+    assert bench.algorithmic_bytes(1, 4096, 4096, 2, -0.25) == 33_595_392
+    assert WORKLOADS["f32_4096"].flops == int(g["flops"])
+    assert WORKLOADS["bf16_8192"].flops == 1_099_511_627_776
+    assert WORKLOADS["bf16_mlp"].flops == 962_072_674_304
+
+
+def test_roofline_is_min_of_peak_and_intensity_times_bandwidth():
+    # intensity 0.5 FLOP/B at 6680.8 GB/s -> 3.34 TFLOP/s, below any peak
+    assert bench.roofline_tflops(1.0, 2.0, 1886.0, 6680.8) == pytest.approx(3.3404)
+    assert bench.roofline_tflops(2048.0, 1.0, 1886.0, 6680.8) == 1886.0
+    # the page's hypothetical machine: P = 20 TFLOP/s, BW = 1 TB/s, T = 64 tile
+    q64 = 8657043456
+    assert bench.roofline_tflops(137438953472, q64, 20.0, 1000.0) == pytest.approx(15.875969, abs=1e-6)
+
+
+def test_fp32_peak_formula():
+    assert bench.fp32_core_peak_tflops(152, 2070.0) == pytest.approx(80.54784)
+
+
+def test_clock_summary():
+    rows = [{"sm": 2070.0, "max": 2070.0, "power": 150.0, "reasons": []},
+            {"sm": 1900.0, "max": 2070.0, "power": 1200.0, "reasons": ["sw_power_cap"]},
+            {"sm": 1950.0, "max": 2070.0, "power": 1100.0, "reasons": []}]
+    c = bench.clock_summary(rows)
+    assert c["sm_mhz"] == 1925.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    assert bench.clock_summary([]) is None
+
+
+def test_committed_traffic_needs_matching_source(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "kern", "k.cu")
+    digest = bench.source_digest("k.cu")
+    (tmp_path / "profiles" / "kern_w_traffic.md").write_text(
+        f"traffic_bytes_per_launch: 123456\nsource_sha256_16: {digest}\n")
+    assert bench.committed_traffic("kern", "w") == 123456.0
+    src.write_text("kernel v2")  # the kernel changed since the capture
+    assert bench.committed_traffic("kern", "w") is None
+    assert bench.committed_traffic("kern", "other") is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elapsed = [3.5, 7.25][rank]
+        got = bench.max_over_ranks(elapsed, world, torch.device("cpu"))
+        bench.barrier(world)
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 7.25, 1: 7.25}
