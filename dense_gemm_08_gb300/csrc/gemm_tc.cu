@@ -8,15 +8,15 @@
 //     ("GEMM on NVIDIA GPUs", section 4, "Tensor Core pipeline": on
 //     Blackwell tcgen05.mma keeps the accumulator in TMEM and takes B from
 //     shared memory).
-//   * TMA fills a STAGES-deep ring of 128-byte-swizzled A/B tiles; full/empty
+//   * TMA fills a multi-stage ring of 128-byte-swizzled A/B tiles; full/empty
 //     mbarriers hand each stage from the load warp to the MMA warp and back
 //     ("Worklog: optimising GEMM on NVIDIA H100", kernel 7 TMA + barriers,
 //     and the producer/consumer pipeline after kernel 8).
 //   * Warp roles: warp 0 issues TMA (one lane), warp 1 owns TMEM and issues
 //     tcgen05.mma (one lane), warps 2-5 run the epilogue.
-//   * Persistent grid (one CTA per SM), static round-robin over output tiles
-//     in grouped order along M so that CTAs running together share A and B
-//     panels in L2 ("GEMM on NVIDIA GPUs", section 5 / grouped schedulers).
+//   * Persistent grid, static round-robin over output tiles in grouped order
+//     along M so that tiles running together share A and B panels in L2
+//     ("GEMM on NVIDIA GPUs", section 5 / grouped schedulers).
 //   * Two TMEM accumulators (2 x 256 columns): the epilogue of tile i runs
 //     while the MMA warp accumulates tile i + 1.
 //   * Epilogue: tcgen05.ld TMEM -> registers, D = alpha * acc + beta * C
@@ -26,8 +26,16 @@
 //     in a device status word, the CTA drains what it has in flight, frees
 //     TMEM and exits.
 //
-// Tile: BM x BN x BK = 128 x 256 x 64; one tcgen05.mma is 128 x 256 x 16,
-// four per K block.  A stage holds 16 KiB of A and 32 KiB of B.
+// Two variants (template parameter CG, the tcgen05 CTA group):
+//   CG = 1: one CTA per tile of 128 x 256; each 128 x 256 x 16 MMA reads
+//           4 KiB of A and 8 KiB of B from the CTA's shared memory.
+//   CG = 2: a cluster of two CTAs on neighbouring SMs shares a 256 x 256
+//           tile (tcgen05 cta_group::2).  Each CTA loads its own 128 rows of
+//           A and its own 128 columns of B (no multicast); the MMA, issued
+//           by the even CTA, reads both CTAs' shared memory and writes each
+//           CTA's 128 rows of the accumulator into that CTA's TMEM.  Shared
+//           memory traffic per MMA and L2 traffic for B halve, and a stage
+//           shrinks to 32 KiB, so six stages fit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,20 +47,26 @@
 namespace gemm {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;  // 64 BF16 = 128 bytes = one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;  // tile width = MMA N
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
 constexpr int NUM_THREADS = 192;          // 6 warps
-constexpr int kGroupM = 8;
-// ring + barriers + slack for aligning the ring to 1024 bytes
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int kGroupM = 16;               // grouped raster width (tile rows)
+
+template <int CG>
+struct Cfg {
+    static constexpr int TILE_M = BM * CG;  // tile rows covered by the CTA group
+    static constexpr int B_ROWS = BN / CG;  // B columns (N) held by each CTA
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    // ring + barriers + slack for aligning the ring to 1024 bytes
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
 
 __device__ int g_tc_status;  // 0 = fine, 1 = a bounded wait ran out
 
@@ -80,6 +94,24 @@ __device__ __forceinline__ uint64_t global_timer() {
     return t;
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -91,6 +123,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster (address from map_to_rank).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -126,13 +164,24 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag) {
     atomicExch(&g_tc_status, 1);
 }
 
+// 2-D tiled TMA load into this CTA's shared memory; completion is signalled
+// on `bar`.  CG = 2: `bar` may live in the peer CTA (cluster address).
+template <int CG>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0,
                                             int32_t c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
+    if constexpr (CG == 1) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -142,20 +191,83 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Arrive on `bar` once all tcgen05 operations issued so far by this thread
+// have completed.  CG = 2: on the barrier at the same offset in both CTAs.
+template <int CG>
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
+    if constexpr (CG == 1) {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    } else {
+        const uint16_t both = 0x3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(both)
+            : "memory");
+    }
 }
 
+// Arrive on this CTA's `bar` once all tcgen05 operations issued so far by
+// this thread have completed (a kernel may use only one CTA-group size).
+template <int CG>
+__device__ __forceinline__ void tc_commit_local(uint32_t bar) {
+    if constexpr (CG == 1) {
+        tc_commit<1>(bar);
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    }
+}
+
+template <int CG>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot) {
+    if constexpr (CG == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
+    if constexpr (CG == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM words: thread t of the warp gets its
@@ -207,10 +319,10 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 // Instruction descriptor, kind::f16: D FP32 (bits 4-5 = 1), A and B BF16
 // (bits 7-9 = 1, 10-12 = 1), A/B major-ness (bit 15 / 16: 0 = K-major,
 // 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc(int a_mn_major, int b_mn_major) {
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn_major, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
-           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-           (static_cast<uint32_t>(BM >> 4) << 24);
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t &tm,
@@ -260,34 +372,40 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs &args, const uint32
 }
 
 // ------------------------------------------------------------------- kernel
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const TcArgs args) {
+    using C = Cfg<CG>;
     extern __shared__ uint8_t smem_raw[];
     // the ring must be 1024-byte aligned for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *full = bars;                  // [STAGES]  TMA -> MMA
-    uint64_t *empty = bars + STAGES;        // [STAGES]  MMA -> TMA
-    uint64_t *tfull = bars + 2 * STAGES;    // [2]       MMA -> epilogue
-    uint64_t *tempty = tfull + ACC_BUFS;    // [2]       epilogue -> MMA
-    uint64_t *drain = tempty + ACC_BUFS;    // [1]       MMA teardown
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t *full = bars;                   // [STAGES]  TMA -> MMA (leader counts both CTAs)
+    uint64_t *empty = bars + C::STAGES;      // [STAGES]  MMA -> TMA
+    uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
+    uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
+    uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const uint32_t rank = CG == 1 ? 0u : cluster_rank();  // position in the CTA pair
+    const bool leader = rank == 0;
+    const int64_t group_id = blockIdx.x / CG;  // tile-group (pair) index
+    const int64_t num_groups = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(smem_addr(&tfull[b]), 1);
-            mbar_init(smem_addr(&tempty[b]), 4);  // one arrival per epilogue warp
+            mbar_init(smem_addr(&tempty[b]), 4 * CG);  // one arrival per epilogue warp of the group
         }
         mbar_init(smem_addr(drain), 1);
         *abort_flag = 0;
@@ -298,20 +416,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b))
                      : "memory");
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<CG>(smem_addr(tmem_slot));
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int64_t n_tiles = args.tiles_m * args.tiles_n;
     const uint32_t ring_base = smem_addr(ring);
+    bool aborted = false;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -320,11 +434,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            for (int64_t t = group_id; t < n_tiles && ok; t += num_groups) {
                 int64_t tm, tn;
                 tile_coords(t, args, tm, tn);
-                const int32_t m0 = static_cast<int32_t>(tm * BM);
-                const int32_t n0 = static_cast<int32_t>(tn * BN);
+                const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
+                const int32_t n0 = static_cast<int32_t>(tn * BN + rank * C::B_ROWS);
                 for (int64_t kb = 0; kb < args.num_kb; ++kb) {
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                       args.timeout_ns)) {
@@ -332,25 +446,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_addr(&full[stage]);
-                    const uint32_t sa = ring_base + stage * STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint32_t fb_local = smem_addr(&full[stage]);
+                    // the leader's full barrier counts both CTAs' bytes
+                    const uint32_t fb = CG == 1 ? fb_local : map_to_rank(fb_local, 0);
+                    const uint32_t sa = ring_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
                     const int32_t k0 = static_cast<int32_t>(kb * BK);
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(fb_local, CG * C::STAGE_BYTES);
                     if (args.a_kmajor) {
-                        tma_load_2d(sa, &map_a, k0, m0, fb);
+                        tma_load_2d<CG>(sa, &map_a, k0, m0, fb);
                     } else {
                         for (int i = 0; i < BM / 64; ++i)
-                            tma_load_2d(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
+                            tma_load_2d<CG>(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
                     }
                     if (args.b_kmajor) {
-                        tma_load_2d(sb, &map_b, k0, n0, fb);
+                        tma_load_2d<CG>(sb, &map_b, k0, n0, fb);
                     } else {
-                        for (int i = 0; i < BN / 64; ++i)
-                            tma_load_2d(sb + i * 64 * 128, &map_b, n0 + 64 * i, k0, fb);
+                        for (int i = 0; i < C::B_ROWS / 64; ++i)
+                            tma_load_2d<CG>(sb + i * 64 * 128, &map_b, n0 + 64 * i, k0, fb);
                     }
                     ++issued;
-                    if (++stage == STAGES) {
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -358,35 +474,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             // Let the copies still in flight land before the CTA can exit:
             // wait on the full barrier of each of the last issued stages.
-            const int64_t outstanding = issued < STAGES ? issued : STAGES;
-            int s = stage;
-            uint32_t ph = phase;
-            for (int64_t i = 0; i < outstanding; ++i) {
-                if (--s < 0) {
-                    s = STAGES - 1;
-                    ph ^= 1;
+            // CG = 2: the leader's full barriers also count the peer's bytes,
+            // so the leader's drain covers both CTAs' copies.
+            if (leader) {
+                const int64_t outstanding = issued < C::STAGES ? issued : C::STAGES;
+                int s = stage;
+                uint32_t ph = phase;
+                for (int64_t i = 0; i < outstanding; ++i) {
+                    if (--s < 0) {
+                        s = C::STAGES - 1;
+                        ph ^= 1;
+                    }
+                    const volatile int never = 0;  // issued copies complete regardless of aborts
+                    if (!wait_bounded(smem_addr(&full[s]), ph, &never, args.timeout_ns))
+                        raise_abort(abort_flag);
                 }
-                // bounded, and independent of the abort flag: the copies were issued
-                const volatile int never = 0;
-                if (!wait_bounded(smem_addr(&full[s]), ph, &never, args.timeout_ns))
-                    raise_abort(abort_flag);
             }
+            aborted = !ok;
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc(!args.a_kmajor, !args.b_kmajor);
+        if (lane == 0 && leader) {
+            const uint32_t idesc = make_idesc(C::TILE_M, BN, !args.a_kmajor, !args.b_kmajor);
             int stage = 0;
             uint32_t phase = 0;
             int64_t li = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++li) {
+            for (int64_t t = group_id; t < n_tiles && ok; t += num_groups, ++li) {
                 const int buf = static_cast<int>(li & 1);
                 const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
                 if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
                                   args.timeout_ns)) {
                     raise_abort(abort_flag);
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
@@ -399,28 +520,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = ring_base + stage * STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint32_t sa = ring_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = args.a_kmajor ? desc_kmajor(sa, kk) : desc_mnmajor(sa, kk);
                         const uint64_t bd = args.b_kmajor ? desc_kmajor(sb, kk) : desc_mnmajor(sb, kk);
-                        tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma<CG>(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(smem_addr(&empty[stage]));  // frees the stage when these MMAs finish
-                    if (++stage == STAGES) {
+                    tc_commit<CG>(smem_addr(&empty[stage]));  // frees the stage (in both CTAs)
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_addr(&tfull[buf]));  // accumulator ready for the epilogue
+                tc_commit<CG>(smem_addr(&tfull[buf]));  // accumulator ready for the epilogue(s)
             }
-            // all MMAs this thread issued have finished once `drain` completes
-            tc_commit(smem_addr(drain));
+            // all MMAs issued here have finished once `drain` completes
+            tc_commit_local<CG>(smem_addr(drain));
             const volatile int never = 0;
             if (!wait_bounded(smem_addr(drain), 0, &never, args.timeout_ns))
                 raise_abort(abort_flag);
+            aborted = !ok;
         }
         __syncwarp();
     } else {
@@ -429,7 +551,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool use_c = args.beta != 0.f;
         int64_t li = 0;
-        for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++li) {
+        for (int64_t t = group_id; t < n_tiles; t += num_groups, ++li) {
             const int buf = static_cast<int>(li & 1);
             const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
             // lane 0 waits, the warp follows its verdict (keeps the warp converged)
@@ -439,12 +561,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) raise_abort(abort_flag);
+                aborted = true;
                 break;
             }
             tc_fence_after();
             int64_t tm, tn;
             tile_coords(t, args, tm, tn);
-            const int64_t row = tm * BM + quarter * 32 + lane;
+            const int64_t row = tm * C::TILE_M + rank * BM + quarter * 32 + lane;
             const bool row_ok = row < args.M;
             float *drow = args.D + row * args.ldd;
             const float *crow = use_c ? args.C + row * args.ldc : nullptr;
@@ -458,7 +581,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // accumulator buffer fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(&tempty[buf]));
+                    if (lane == 0) {
+                        const uint32_t te = smem_addr(&tempty[buf]);
+                        if (CG == 1)
+                            mbar_arrive(te);
+                        else
+                            mbar_arrive_cluster(map_to_rank(te, 0));
+                    }
                 }
                 const int64_t c0 = tn * BN + chunk * 32;
                 if (row_ok && c0 < args.N) store_row_chunk(args, v, drow, crow, c0, use_c);
@@ -466,14 +595,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    if (aborted) {
+        // give copies issued by a peer that gave up a short time to land
+        const uint64_t t0 = global_timer();
+        while (global_timer() - t0 < 2000000ull) __nanosleep(1000);
+    }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // the pair's MMAs and remote arrivals are done
     tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
-    }
+    if (warp == 1) tmem_dealloc<CG>(tmem_base);
 }
 
 // ---------------------------------------------------------------- host side
@@ -509,16 +640,87 @@ bool encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[kMaxDevices];
 
-int device_sm_count(int dev) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-    return n > 0 ? n : 1;
-}
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sms = 1;
+    int pairs = 0;  // CTA pairs that can be resident at once (0: pair variant not used)
+};
+DeviceInfo g_dev[kMaxDevices];
 
 bool aligned(const void *ptr, size_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) % bytes) == 0;
+}
+
+cudaLaunchConfig_t launch_config(int grid, int cg, size_t smem, cudaStream_t stream,
+                                 cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = static_cast<unsigned>(cg);
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Per device, once: opt in to the large shared-memory carve-out and find how
+// many CTA pairs can be resident at once.
+DeviceInfo *device_info(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceInfo *d = &g_dev[dev];
+    std::call_once(d->once, [d, dev] {
+        int n = 0;
+        d->err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (d->err != cudaSuccess) return;
+        d->sms = n > 0 ? n : 1;
+        d->err = cudaFuncSetAttribute(gemm_bf16_tc_kernel<1>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<1>::SMEM_BYTES);
+        if (d->err != cudaSuccess) return;
+        d->err = cudaFuncSetAttribute(gemm_bf16_tc_kernel<2>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<2>::SMEM_BYTES);
+        if (d->err != cudaSuccess) return;
+        cudaLaunchAttribute attr;
+        cudaLaunchConfig_t cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2>::SMEM_BYTES, 0, &attr);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_tc_kernel<2>, &cfg) !=
+            cudaSuccess) {
+            clusters = 0;
+            (void)cudaGetLastError();  // clear it: the pair variant is then not used
+        }
+        d->pairs = clusters;
+    });
+    return d;
+}
+
+template <int CG>
+cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStream_t stream) {
+    using C = Cfg<CG>;
+    CUtensorMap map_a, map_b;
+    bool ok;
+    if (p.a_kmajor)  // A(i, k) at A[i * lda + k]: inner K, outer M; box 64 K x 128 rows
+        ok = encode_2d(&map_a, p.A, p.K, p.M, p.lda, BK, BM);
+    else  // A(i, k) at A[i + k * lda]: inner M, outer K; boxes of 64 M x 64 K
+        ok = encode_2d(&map_a, p.A, p.M, p.K, p.lda, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+    if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N; box 64 K x B_ROWS
+        ok = encode_2d(&map_b, p.B, p.K, p.N, p.ldb, BK, C::B_ROWS);
+    else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
+        ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+    TcArgs a = a0;
+    a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
+    a.tiles_n = (p.N + BN - 1) / BN;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr);
+    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, a);
 }
 
 }  // namespace
@@ -536,29 +738,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices && !g_attr_done[dev].load()) {
-        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        g_attr_done[dev].store(1);
-    } else if (dev >= kMaxDevices) {
-        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-    }
-
-    CUtensorMap map_a, map_b;
-    bool ok;
-    if (p.a_kmajor)  // A(i, k) at A[i * lda + k]: inner K, outer M
-        ok = encode_2d(&map_a, p.A, p.K, p.M, p.lda, BK, BM);
-    else  // A(i, k) at A[i + k * lda]: inner M, outer K
-        ok = encode_2d(&map_a, p.A, p.M, p.K, p.lda, 64, BK);
-    if (!ok) return cudaErrorInvalidValue;
-    if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N
-        ok = encode_2d(&map_b, p.B, p.K, p.N, p.ldb, BK, BN);
-    else  // B(k, j) at B[k * ldb + j]: inner N, outer K
-        ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
-    if (!ok) return cudaErrorInvalidValue;
+    DeviceInfo *d = device_info(dev);
+    if (d == nullptr) return cudaErrorInvalidDevice;
+    if (d->err != cudaSuccess) return d->err;
 
     TcArgs a;
     a.M = p.M;
@@ -570,8 +752,6 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.ldc = p.ldc;
     a.D = p.D;
     a.ldd = p.ldd;
-    a.tiles_m = (p.M + BM - 1) / BM;
-    a.tiles_n = (p.N + BN - 1) / BN;
     a.num_kb = (p.K + BK - 1) / BK;
     a.a_kmajor = p.a_kmajor ? 1 : 0;
     a.b_kmajor = p.b_kmajor ? 1 : 0;
@@ -579,11 +759,19 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.vec_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 
-    const int64_t tiles = a.tiles_m * a.tiles_n;
-    const int64_t sms = device_sm_count(dev);
-    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_a, map_b, a);
-    *name = "gemm_bf16_tc";
+    // CTA pairs when there are at least as many 256 x 256 tiles as resident
+    // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
+    const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
+    if (d->pairs > 0 && pair_tiles >= d->pairs) {
+        *name = "gemm_bf16_tc<pair>";
+        e = launch_variant<2>(p, a, 2 * d->pairs, stream);
+    } else {
+        const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+        const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
+        *name = "gemm_bf16_tc";
+        e = launch_variant<1>(p, a, grid, stream);
+    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

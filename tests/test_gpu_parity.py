@@ -71,7 +71,7 @@ def test_full_size_config_sampled(name):
     ratio, kernel = sampled_check(w, inp, rows=(0, 1, w.M // 2 + 3, w.M - 1),
                                   cols=(0, w.N // 3 + 1, w.N - 1))
     if w.dtype == "bf16":
-        assert kernel == "gemm_bf16_tc"
+        assert kernel == "gemm_bf16_tc<pair>"
 
 
 @pytest.mark.parametrize("name", sorted(k for k in WORKLOADS if k.startswith("odd_")))
@@ -96,6 +96,28 @@ def test_all_orders_full(dtype, orders):
     inp = make_inputs(w, seed=1, pad=3, ld_multiple=8)
     expect = "gemm_bf16_tc" if dtype == "bf16" else "sgemm_simt<f32"
     full_check(w, inp, pad_d=5, expect_kernel=expect)
+
+
+# Big enough for the CTA-pair variant (>= 100 tiles of 256 x 256), ragged in
+# M, N and K, so both CTAs of a pair see partial tiles.
+PAIR_SHAPE = (2500, 2600, 136)
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_cta_pair_variant_all_orders_full(orders):
+    M, N, K = PAIR_SHAPE
+    w = Workload("pair", M, N, K, 1.5, -0.25, "bf16", *orders)
+    inp = make_inputs(w, seed=11, pad=5, ld_multiple=8)
+    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair>")
+
+
+def test_cta_pair_variant_small_integers_bit_exact():
+    w = Workload("pair_int", 2304, 2560, 1000, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
+    inp = make_inputs(w, seed=12)
+    Dbuf, _, name = run_gpu(w, inp)
+    assert name == "gemm_bf16_tc<pair>"
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
 
 
 @pytest.mark.parametrize("shape", [(257, 515, 1000), (128, 256, 64), (1, 1, 1), (129, 1, 77),
