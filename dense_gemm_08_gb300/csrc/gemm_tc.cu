@@ -64,8 +64,10 @@ struct Cfg {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = CG == 1 ? 4 : 6;
-    // ring + barriers + slack for aligning the ring to 1024 bytes
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    // epilogue staging: per epilogue warp two 32 x 32 FP32 boxes (4 KiB each)
+    static constexpr int STAGING_BYTES = 4 * 2 * 32 * 32 * 4;
+    // ring + staging + barriers + slack for aligning the ring to 1024 bytes
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
 
 __device__ int g_tc_status;  // 0 = fine, 1 = a bounded wait ran out
@@ -80,6 +82,7 @@ struct TcArgs {
     int64_t tiles_m, tiles_n, num_kb;
     int a_kmajor, b_kmajor;
     int vec_c, vec_d;
+    int tma_d;  // D is written through TMA boxes (16-byte aligned base and pitch)
     uint64_t timeout_ns;
 };
 
@@ -182,6 +185,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
             "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
             : "memory");
     }
+}
+
+// 2-D tiled TMA store of a shared-memory box to global memory (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t c0, int32_t c1,
+                                             uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N bulk groups of this thread are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -335,6 +358,32 @@ __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t 
     tn = (t % width) / gsz;
 }
 
+// o[j] = alpha * acc[j] + beta * C[row, c0 + j] for one thread's 32 columns
+// (C read only when use_c; columns past N are left as alpha * acc).
+__device__ __forceinline__ void epilogue_values(const TcArgs &args, const uint32_t (&v)[32],
+                                                const float *crow, int64_t c0, bool use_c,
+                                                bool row_ok, float (&o)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+    if (!use_c || !row_ok) return;
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const int64_t col = c0 + j4 * 4;
+        if (col + 3 < args.N && args.vec_c) {
+            // plain load: C may be D itself (in-place update)
+            const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+            o[j4 * 4 + 0] = fmaf(args.beta, c.x, o[j4 * 4 + 0]);
+            o[j4 * 4 + 1] = fmaf(args.beta, c.y, o[j4 * 4 + 1]);
+            o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
+            o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (col + j < args.N) o[j4 * 4 + j] = fmaf(args.beta, crow[col + j], o[j4 * 4 + j]);
+        }
+    }
+}
+
 // D[row, c0 .. c0+31] = alpha * acc + beta * C[row, ...] for one thread's row,
 // with 16-byte accesses where the row allows and per-element guards at the edge.
 __device__ __forceinline__ void store_row_chunk(const TcArgs &args, const uint32_t (&v)[32],
@@ -375,14 +424,16 @@ __device__ __forceinline__ void store_row_chunk(const TcArgs &args, const uint32
 template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_b, const TcArgs args) {
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_d, const TcArgs args) {
     using C = Cfg<CG>;
     extern __shared__ uint8_t smem_raw[];
     // the ring must be 1024-byte aligned for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t *staging = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned, 4 warps x 2 x 4 KiB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
     uint64_t *full = bars;                   // [STAGES]  TMA -> MMA (leader counts both CTAs)
     uint64_t *empty = bars + C::STAGES;      // [STAGES]  MMA -> TMA
     uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
@@ -415,6 +466,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b))
                      : "memory");
+        if (args.tma_d)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d))
+                         : "memory");
     }
     if (warp == 1) tmem_alloc<CG>(smem_addr(tmem_slot));
     tc_fence_before();
@@ -550,6 +604,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp % 4;  // TMEM lanes this warp may access
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool use_c = args.beta != 0.f;
+        uint32_t slab_chunks = 0;  // boxes this warp has staged (selects the staging buffer)
         int64_t li = 0;
         for (int64_t t = group_id; t < n_tiles; t += num_groups, ++li) {
             const int buf = static_cast<int>(li & 1);
@@ -572,6 +627,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float *drow = args.D + row * args.ldd;
             const float *crow = use_c ? args.C + row * args.ldc : nullptr;
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
+            const int64_t row0 = row - lane;  // first row of this warp's 32-row slab
 #pragma unroll 1
             for (int chunk = 0; chunk < BN / 32; ++chunk) {
                 uint32_t v[32];
@@ -590,9 +646,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 const int64_t c0 = tn * BN + chunk * 32;
-                if (row_ok && c0 < args.N) store_row_chunk(args, v, drow, crow, c0, use_c);
+                if (c0 >= args.N || row0 >= args.M) continue;  // warp-uniform
+                if (args.tma_d) {
+                    // Stage the 32 x 32 box in shared memory with the 128-byte
+                    // swizzle (16-byte chunk j of row r at position j ^ (r % 8):
+                    // conflict-free) and write it with one TMA store: full
+                    // 128-byte lines instead of 16-byte pieces of 32 rows.
+                    float o[32];
+                    epilogue_values(args, v, crow, c0, use_c, row_ok, o);
+                    const int sb = (slab_chunks++) & 1;
+                    uint8_t *box = staging + (quarter * 2 + sb) * 4096;
+                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float4 *dst = reinterpret_cast<float4 *>(box + lane * 128 +
+                                                                 ((j4 ^ (lane & 7)) * 16));
+                        *dst = make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2],
+                                           o[j4 * 4 + 3]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        tma_store_2d(&map_d, static_cast<int32_t>(c0), static_cast<int32_t>(row0),
+                                     smem_addr(box));
+                } else if (row_ok) {
+                    store_row_chunk(args, v, drow, crow, c0, use_c);
+                }
             }
         }
+        if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+        __syncwarp();
     }
 
     if (aborted) {
@@ -715,12 +799,26 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
         ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
+    // D: FP32 row-major M x N; 32 x 32 boxes with the 128-byte swizzle
+    CUtensorMap map_d;
     TcArgs a = a0;
+    if (a.tma_d) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ldd) * 4};
+        cuuint32_t box[2] = {32, 32};
+        cuuint32_t estr[2] = {1, 1};
+        const CUresult r = g_encode(&map_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.D, dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) a.tma_d = 0;
+    }
+    if (!a.tma_d) map_d = map_a;  // unused placeholder
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr);
-    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, a);
+    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, map_d, a);
 }
 
 }  // namespace
@@ -757,6 +855,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.b_kmajor = p.b_kmajor ? 1 : 0;
     a.vec_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
     a.vec_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
+    a.tma_d = a.vec_d;  // TMA needs a 16-byte aligned base and a pitch of whole 16 bytes
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
