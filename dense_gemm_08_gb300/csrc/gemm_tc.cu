@@ -54,7 +54,7 @@ constexpr int BN = 256;  // tile width = MMA N
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
 constexpr int NUM_THREADS = 192;          // 6 warps
-constexpr int kGroupM = 16;               // grouped raster width (tile rows)
+constexpr int kGroupM = 8;                // grouped raster width (tile rows)
 
 template <int CG>
 struct Cfg {

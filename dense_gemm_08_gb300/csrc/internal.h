@@ -27,6 +27,12 @@ struct Problem {
 
 enum class InType { F32, BF16 };
 
+// Temporary device workspace from a library-owned, stream-ordered memory pool
+// (one per device, kept warm between calls): memory handed out on `stream`
+// and returned on `stream` once the kernels enqueued before the free are done.
+cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr);
+cudaError_t workspace_free(void *ptr, cudaStream_t stream);
+
 // Each launcher enqueues one kernel on `stream`, returns the CUDA error of
 // the launch and sets *name to the kernel's static name.
 cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name);

@@ -52,8 +52,9 @@ struct SimtCfg {
     static_assert(BK % 4 == 0, "K slices hold whole vectors");
 };
 
-// 128 x 128 x 8 tile, 256 threads, 8 x 8 per thread, two CTAs per SM.
-using BigCfg = SimtCfg<128, 128, 8, 2, 4, 8, 4, 2, 2, 2>;
+// 128 x 256 x 16 tile, 256 threads, 8 x 16 per thread (warp tile 64 x 64),
+// one CTA per SM: 128 FMAs per 6 fragment loads.
+using BigCfg = SimtCfg<128, 256, 16, 2, 4, 8, 4, 2, 4, 1>;
 // 64 x 64 x 16 tile, 256 threads, 4 x 4 per thread: more CTAs for small problems.
 using SmallCfg = SimtCfg<64, 64, 16, 2, 4, 8, 4, 1, 1, 1>;
 
@@ -82,19 +83,18 @@ struct Elem<uint16_t> {
     }
 };
 
-// Fetch this thread's share of one BK-slice of an operand X into registers.
-// X(mn, k) is at X[mn * ld + k] when KMAJ, else at X[mn + k * ld].
-// Each share is SLOTS vectors of 4 consecutive elements along X's contiguous
-// dimension.  `vec`: 16-byte (FP32) / 8-byte (BF16) vector loads are aligned.
-// `guard`: the slice may cross the matrix edge (out-of-range elements are 0).
+// Per-thread view of one operand's slices.  X(mn, k) is at X[mn * ld + k]
+// when KMAJ, else at X[mn + k * ld].  The thread owns SLOTS vectors of 4
+// consecutive elements along X's contiguous dimension in every BK-slice; their
+// addresses at k = 0 are computed once per tile, and each slice moves them by
+// `kstep` elements.
 template <typename T, bool KMAJ, int EXT, int BK, int NT, int SLOTS>
-__device__ __forceinline__ void fetch_slice(float4 (&r)[SLOTS], const T *__restrict__ X,
-                                            int64_t ld, int64_t mn0, int64_t k0, int64_t mn_lim,
-                                            int64_t k_lim, bool vec, bool guard) {
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
+struct SliceLoader {
+    const T *p0[SLOTS];
+    int64_t kstep;
+
+    __device__ __forceinline__ static void coords(int s, int &mn, int &kk) {
         const int v = static_cast<int>(threadIdx.x) + s * NT;
-        int mn, kk;
         if (KMAJ) {
             mn = v / (BK / 4);
             kk = (v % (BK / 4)) * 4;
@@ -102,34 +102,55 @@ __device__ __forceinline__ void fetch_slice(float4 (&r)[SLOTS], const T *__restr
             kk = v / (EXT / 4);
             mn = (v % (EXT / 4)) * 4;
         }
-        const int64_t gm = mn0 + mn, gk = k0 + kk;
-        const T *ptr = KMAJ ? X + gm * ld + gk : X + gk * ld + gm;
-        // elements of the vector step along the contiguous dimension
-        const int64_t lead = KMAJ ? gk : gm, lead_lim = KMAJ ? k_lim : mn_lim;
-        const bool row_ok = KMAJ ? (gm < mn_lim) : (gk < k_lim);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!guard) {
-            if (vec) {
-                x = Elem<T>::four(ptr);
-            } else {
-                x.x = Elem<T>::one(ptr);
-                x.y = Elem<T>::one(ptr + 1);
-                x.z = Elem<T>::one(ptr + 2);
-                x.w = Elem<T>::one(ptr + 3);
-            }
-        } else if (row_ok) {
-            if (vec && lead + 3 < lead_lim) {
-                x = Elem<T>::four(ptr);
-            } else {
-                if (lead + 0 < lead_lim) x.x = Elem<T>::one(ptr);
-                if (lead + 1 < lead_lim) x.y = Elem<T>::one(ptr + 1);
-                if (lead + 2 < lead_lim) x.z = Elem<T>::one(ptr + 2);
-                if (lead + 3 < lead_lim) x.w = Elem<T>::one(ptr + 3);
-            }
-        }
-        r[s] = x;
     }
-}
+
+    __device__ __forceinline__ void init(const T *X, int64_t ld, int64_t mn0) {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            int mn, kk;
+            coords(s, mn, kk);
+            p0[s] = KMAJ ? X + (mn0 + mn) * ld + kk : X + static_cast<int64_t>(kk) * ld + mn0 + mn;
+        }
+        kstep = KMAJ ? BK : BK * ld;
+    }
+
+    // Interior slice with aligned vectors: one wide load per slot.
+    __device__ __forceinline__ void fetch_fast(float4 (&r)[SLOTS], int64_t kt) const {
+        const int64_t off = kt * kstep;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) r[s] = Elem<T>::four(p0[s] + off);
+    }
+
+    // Any slice: per-element guards (out-of-range elements are 0); wide loads
+    // only when `vec` says they are aligned.
+    __device__ __forceinline__ void fetch_guarded(float4 (&r)[SLOTS], int64_t kt, int64_t mn0,
+                                                  int64_t mn_lim, int64_t k_lim,
+                                                  bool vec) const {
+        const int64_t off = kt * kstep;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            int mn, kk;
+            coords(s, mn, kk);
+            const int64_t gm = mn0 + mn, gk = kt * BK + kk;
+            const T *ptr = p0[s] + off;
+            // elements of the vector step along the contiguous dimension
+            const int64_t lead = KMAJ ? gk : gm, lead_lim = KMAJ ? k_lim : mn_lim;
+            const bool row_ok = KMAJ ? (gm < mn_lim) : (gk < k_lim);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row_ok) {
+                if (vec && lead + 3 < lead_lim) {
+                    x = Elem<T>::four(ptr);
+                } else {
+                    if (lead + 0 < lead_lim) x.x = Elem<T>::one(ptr);
+                    if (lead + 1 < lead_lim) x.y = Elem<T>::one(ptr + 1);
+                    if (lead + 2 < lead_lim) x.z = Elem<T>::one(ptr + 2);
+                    if (lead + 3 < lead_lim) x.w = Elem<T>::one(ptr + 3);
+                }
+            }
+            r[s] = x;
+        }
+    }
+};
 
 // Write the fetched share into shared memory laid out as [BK][EXT + PAD].
 template <bool KMAJ, int EXT, int BK, int NT, int SLOTS, int STRIDE>
@@ -155,6 +176,17 @@ struct SimtArgs {
     bool vec_a, vec_b;  // vector global loads of A / B are aligned
     bool vec_c, vec_d;  // 16-byte accesses of C / D rows are aligned
     int64_t tiles_m, tiles_n;
+    // Stream-K tail: tiles [0, full_tiles) are computed whole, one per CTA;
+    // the remaining tail_tiles x n_k slice-iterations are dealt out evenly, in
+    // order, to sk_ctas CTAs.  A CTA holding only part of a tile's K range
+    // stores its partial sums in ws_part (slot = its position among the
+    // tile's contributors, which are in K order) and counts itself in
+    // ws_count; the last contributor adds the partials in that order and
+    // writes D.
+    int64_t full_tiles, tail_iters;
+    int sk_ctas, max_contrib;
+    float *ws_part;
+    int *ws_count;
 };
 
 constexpr int kGroupM = 8;  // grouped raster: 8 tile-rows share each B column panel
@@ -176,10 +208,39 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
     const int a_off = wm * Cfg::WTM + tr * 4;  // first row of this thread's quads
     const int b_off = wn * Cfg::WTN + tc * 4;  // first column of this thread's quads
 
-    const int64_t n_tiles = args.tiles_m * args.tiles_n;
     const int64_t n_k = (p.K + BK - 1) / BK;
+    __shared__ int s_last;  // this CTA completed a split tile
 
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t n_units = args.full_tiles + args.sk_ctas;
+    // first stream-K CTA whose range holds tail iteration x
+    auto owner = [&](int64_t x) -> int64_t {
+        return ((x + 1) * args.sk_ctas - 1) / args.tail_iters;
+    };
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+      int64_t it = 0, it_end = 1;  // tail iterations of this unit (stream-K units only)
+      if (u >= args.full_tiles) {
+          const int64_t c = u - args.full_tiles;
+          it = c * args.tail_iters / args.sk_ctas;
+          it_end = (c + 1) * args.tail_iters / args.sk_ctas;
+      }
+      while (it < it_end) {
+        // this step: one tile and a K range of it
+        int64_t t = u, kt_begin = 0, kt_end = n_k;
+        int contrib = 0, n_contrib = 1;
+        if (u >= args.full_tiles) {
+            const int64_t tl = it / n_k;
+            kt_begin = it % n_k;
+            kt_end = kt_begin + (it_end - it);
+            if (kt_end > n_k) kt_end = n_k;
+            t = args.full_tiles + tl;
+            const int64_t c0 = owner(tl * n_k), c1 = owner(tl * n_k + n_k - 1);
+            contrib = static_cast<int>(u - args.full_tiles - c0);
+            n_contrib = static_cast<int>(c1 - c0 + 1);
+            it += kt_end - kt_begin;
+        } else {
+            it = it_end;  // whole tile
+        }
+        const int split = n_contrib > 1 ? contrib : -1;
         // grouped rasterisation along M
         const int64_t width = kGroupM * args.tiles_n;
         const int64_t first_m = (t / width) * kGroupM;
@@ -196,62 +257,120 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
+        SliceLoader<T, AK, BM, BK, NT, Cfg::SLOTS_A> la;
+        SliceLoader<T, BKM, BN, BK, NT, Cfg::SLOTS_B> lb;
+        la.init(A, p.lda, m0);
+        lb.init(B, p.ldb, n0);
+        // interior tiles with aligned operands take the unguarded wide loads
+        const bool fast_mn = !edge_mn && args.vec_a && args.vec_b;
+        const int64_t full_slices = p.K / BK;  // slices entirely inside K
+
         float4 ra[Cfg::SLOTS_A], rb[Cfg::SLOTS_B];
-        {
-            const bool guard = edge_mn || (BK > p.K);
-            fetch_slice<T, AK, BM, BK, NT, Cfg::SLOTS_A>(ra, A, p.lda, m0, 0, p.M, p.K,
-                                                         args.vec_a, guard);
-            fetch_slice<T, BKM, BN, BK, NT, Cfg::SLOTS_B>(rb, B, p.ldb, n0, 0, p.N, p.K,
-                                                          args.vec_b, guard);
-            stage_slice<AK, BM, BK, NT, Cfg::SLOTS_A, SA>(As[0], ra);
-            stage_slice<BKM, BN, BK, NT, Cfg::SLOTS_B, SB>(Bs[0], rb);
-        }
+        auto fetch = [&](int64_t kt) {
+            if (fast_mn && kt < full_slices) {
+                la.fetch_fast(ra, kt);
+                lb.fetch_fast(rb, kt);
+            } else {
+                la.fetch_guarded(ra, kt, m0, p.M, p.K, args.vec_a);
+                lb.fetch_guarded(rb, kt, n0, p.N, p.K, args.vec_b);
+            }
+        };
+        if (kt_begin < kt_end) {  // CTA-uniform
+        fetch(kt_begin);
+        stage_slice<AK, BM, BK, NT, Cfg::SLOTS_A, SA>(As[0], ra);
+        stage_slice<BKM, BN, BK, NT, Cfg::SLOTS_B, SB>(Bs[0], rb);
         __syncthreads();
 
-        for (int64_t kt = 0; kt < n_k; ++kt) {
-            const int cur = static_cast<int>(kt & 1);
-            const bool more = kt + 1 < n_k;
-            if (more) {
-                const int64_t k0 = (kt + 1) * BK;
-                const bool guard = edge_mn || (k0 + BK > p.K);
-                fetch_slice<T, AK, BM, BK, NT, Cfg::SLOTS_A>(ra, A, p.lda, m0, k0, p.M, p.K,
-                                                             args.vec_a, guard);
-                fetch_slice<T, BKM, BN, BK, NT, Cfg::SLOTS_B>(rb, B, p.ldb, n0, k0, p.N, p.K,
-                                                              args.vec_b, guard);
-            }
+        for (int64_t kt = kt_begin; kt < kt_end; ++kt) {
+            const int cur = static_cast<int>((kt - kt_begin) & 1);
+            const bool more = kt + 1 < kt_end;
+            if (more) fetch(kt + 1);  // lands in registers while this slice is multiplied
             const float *as = As[cur];
             const float *bs = Bs[cur];
-#pragma unroll
-            for (int k = 0; k < BK; ++k) {
-                float a[TM], b[TN];
+            // fragments double-buffered in registers: slice row k + 1 is read
+            // from shared memory while row k is multiplied
+            float a[2][TM], b[2][TN];
+            auto load_frag = [&](int buf, int k) {
 #pragma unroll
                 for (int q = 0; q < Cfg::QM; ++q) {
                     const float4 v =
                         *reinterpret_cast<const float4 *>(&as[k * SA + a_off + q * Cfg::LM * 4]);
-                    a[q * 4 + 0] = v.x;
-                    a[q * 4 + 1] = v.y;
-                    a[q * 4 + 2] = v.z;
-                    a[q * 4 + 3] = v.w;
+                    a[buf][q * 4 + 0] = v.x;
+                    a[buf][q * 4 + 1] = v.y;
+                    a[buf][q * 4 + 2] = v.z;
+                    a[buf][q * 4 + 3] = v.w;
                 }
 #pragma unroll
                 for (int q = 0; q < Cfg::QN; ++q) {
                     const float4 v =
                         *reinterpret_cast<const float4 *>(&bs[k * SB + b_off + q * Cfg::LN * 4]);
-                    b[q * 4 + 0] = v.x;
-                    b[q * 4 + 1] = v.y;
-                    b[q * 4 + 2] = v.z;
-                    b[q * 4 + 3] = v.w;
+                    b[buf][q * 4 + 0] = v.x;
+                    b[buf][q * 4 + 1] = v.y;
+                    b[buf][q * 4 + 2] = v.z;
+                    b[buf][q * 4 + 3] = v.w;
                 }
+            };
+            load_frag(0, 0);
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                if (k + 1 < BK) load_frag((k + 1) & 1, k + 1);
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                    for (int j = 0; j < TN; ++j)
+                        acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
             }
             if (more) {
                 stage_slice<AK, BM, BK, NT, Cfg::SLOTS_A, SA>(As[cur ^ 1], ra);
                 stage_slice<BKM, BN, BK, NT, Cfg::SLOTS_B, SB>(Bs[cur ^ 1], rb);
             }
             __syncthreads();
+        }
+        }
+
+        if (split >= 0) {
+            // Every contributor of a split tile stores its partial sums (each
+            // thread its own TM x TN block), then counts itself; the last one
+            // adds all partials in K order -- the same order whatever the
+            // arrival order, so the result is deterministic -- and runs the
+            // epilogue.
+            const int64_t slot = t - args.full_tiles;
+            float *tile_ws = args.ws_part + slot * args.max_contrib * (BM * BN);
+            float4 *mine = reinterpret_cast<float4 *>(tile_ws + split * (BM * BN) +
+                                                      threadIdx.x * (TM * TN));
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j4 = 0; j4 < TN / 4; ++j4)
+                    __stcg(&mine[i * (TN / 4) + j4],
+                           make_float4(acc[i][j4 * 4 + 0], acc[i][j4 * 4 + 1],
+                                       acc[i][j4 * 4 + 2], acc[i][j4 * 4 + 3]));
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0)
+                s_last = atomicAdd(&args.ws_count[slot], 1) == n_contrib - 1;
+            __syncthreads();
+            if (!s_last) continue;  // CTA-uniform
+            __threadfence();
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+            for (int sp = 0; sp < n_contrib; ++sp) {
+                const float4 *part = reinterpret_cast<const float4 *>(
+                    tile_ws + sp * (BM * BN) + threadIdx.x * (TM * TN));
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j4 = 0; j4 < TN / 4; ++j4) {
+                        const float4 v = __ldcg(&part[i * (TN / 4) + j4]);
+                        acc[i][j4 * 4 + 0] += v.x;
+                        acc[i][j4 * 4 + 1] += v.y;
+                        acc[i][j4 * 4 + 2] += v.z;
+                        acc[i][j4 * 4 + 3] += v.w;
+                    }
+            }
+            if (threadIdx.x == 0) args.ws_count[slot] = 0;  // ready for the next call
         }
 
         // epilogue: D = alpha * acc + beta * C
@@ -292,12 +411,61 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
                 }
             }
         }
+      }
     }
 }
 
 bool aligned(const void *ptr, size_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) % bytes) == 0;
 }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    return n > 0 ? n : 1;
+}
+
+// How to cut the work into CTA units.  With S resident CTAs and T tiles, the
+// last T mod S tiles would run as a partial wave on a fraction of the SMs.
+// Instead their K-slice iterations are dealt out evenly to S CTAs (a
+// stream-K tail; when T < S every tile is dealt out), so every SM finishes at
+// about the same time ("GEMM on NVIDIA GPUs", section 5: split-K / Stream-K
+// for short M/N and tile tails).
+struct SplitPlan {
+    int64_t full_tiles, tail_tiles, tail_iters;
+    int sk_ctas, max_contrib;
+};
+
+template <typename Cfg>
+SplitPlan plan_split(const Problem &p, int64_t tiles) {
+    const int64_t slots = static_cast<int64_t>(sm_count()) * Cfg::MINB;
+    const int64_t n_k = (p.K + Cfg::BK - 1) / Cfg::BK;
+    SplitPlan plan{tiles, 0, 0, 0, 1};
+    const int64_t rem = tiles % slots;
+    if (rem == 0) return plan;
+    const int64_t tail_tiles = rem;
+    const int64_t iters = tail_tiles * n_k;
+    // at least 4 slices per CTA; no point in fewer CTAs than tail tiles
+    int64_t ctas = slots;
+    if (ctas > iters / 4) ctas = iters / 4;
+    if (ctas <= tail_tiles) return plan;  // nothing to gain: keep whole tiles
+    plan.full_tiles = tiles - tail_tiles;
+    plan.tail_tiles = tail_tiles;
+    plan.tail_iters = iters;
+    plan.sk_ctas = static_cast<int>(ctas);
+    // contributors of tile tl: owner(first iteration) .. owner(last iteration)
+    auto owner = [&](int64_t x) { return ((x + 1) * ctas - 1) / iters; };
+    int64_t maxc = 1;
+    for (int64_t tl = 0; tl < tail_tiles; ++tl) {
+        const int64_t c = owner(tl * n_k + n_k - 1) - owner(tl * n_k) + 1;
+        if (c > maxc) maxc = c;
+    }
+    plan.max_contrib = static_cast<int>(maxc);
+    return plan;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 template <typename Cfg, typename T>
 cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name) {
@@ -311,7 +479,33 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name)
     args.tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
     args.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
     const int64_t tiles = args.tiles_m * args.tiles_n;
-    const unsigned grid = static_cast<unsigned>(tiles < 0x7fffffff ? tiles : 0x7fffffff);
+    const SplitPlan plan = plan_split<Cfg>(p, tiles);
+    args.full_tiles = plan.full_tiles;
+    args.tail_iters = plan.tail_iters > 0 ? plan.tail_iters : 1;
+    args.sk_ctas = plan.sk_ctas;
+    args.max_contrib = plan.max_contrib;
+    args.ws_part = nullptr;
+    args.ws_count = nullptr;
+    const int64_t units = plan.full_tiles + plan.sk_ctas;
+
+    // workspace for the dealt-out tiles: partial sums, then one counter per tile
+    void *ws = nullptr;
+    if (plan.tail_tiles > 0) {
+        const size_t part_bytes = align256(static_cast<size_t>(plan.tail_tiles) *
+                                           plan.max_contrib * Cfg::BM * Cfg::BN * sizeof(float));
+        const size_t count_bytes = static_cast<size_t>(plan.tail_tiles) * sizeof(int);
+        cudaError_t e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+        if (e != cudaSuccess) return e;
+        args.ws_part = static_cast<float *>(ws);
+        args.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
+        e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
+        if (e != cudaSuccess) {
+            workspace_free(ws, stream);
+            return e;
+        }
+    }
+
+    const unsigned grid = static_cast<unsigned>(units < 0x7fffffff ? units : 0x7fffffff);
     const bool f32 = sizeof(T) == 4;
     if (p.a_kmajor && p.b_kmajor) {
         sgemm_simt_kernel<Cfg, T, true, true><<<grid, Cfg::NT, 0, stream>>>(args);
@@ -326,14 +520,12 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name)
         sgemm_simt_kernel<Cfg, T, false, false><<<grid, Cfg::NT, 0, stream>>>(args);
         *name = f32 ? "sgemm_simt<f32,A:M,B:N>" : "sgemm_simt<bf16,A:M,B:N>";
     }
-    return cudaGetLastError();
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-    return n > 0 ? n : 1;
+    cudaError_t e = cudaGetLastError();
+    if (ws != nullptr) {
+        const cudaError_t ef = workspace_free(ws, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e;
 }
 
 __global__ void scale_c_kernel(const Problem p) {

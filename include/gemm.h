@@ -24,9 +24,14 @@
  * -------------------------------------------------
  * Ownership: A, B, C and D are device pointers owned by the caller (for
  *   example torch CUDA tensors).  The library keeps no pointer after the call
- *   returns and allocates no device memory on these paths; tensor maps travel
- *   by value in the launch parameters.  The library holds no per-call state
- *   and may be called from several host threads.
+ *   returns; tensor maps travel by value in the launch parameters.  When the
+ *   CUDA-core kernel splits the K range of its last tiles across CTAs (to keep
+ *   every SM busy), it takes a temporary workspace for partial sums (a few
+ *   tens of MiB at most) from a memory pool the library owns, one per device,
+ *   allocated and freed in stream order on `stream`; the pool keeps up to
+ *   256 MiB of freed memory for later calls.  Nothing else is allocated.  The
+ *   library holds no per-call state and may be called from several host
+ *   threads.
  * Asynchrony: the work is enqueued on `stream` (0 = the legacy default
  *   stream) and the call returns without waiting for it.  The caller keeps
  *   the buffers alive until the stream has passed the call.

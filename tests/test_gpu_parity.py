@@ -120,6 +120,46 @@ def test_cta_pair_variant_small_integers_bit_exact():
     assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
 
 
+# Split-K on the CUDA-core path: few tiles (every tile split along K) and a
+# last partial wave (only its tiles split); results must not depend on the
+# order in which the pieces finish.
+@pytest.mark.parametrize("orders", ORDERS)
+def test_split_k_all_tiles_full(orders):
+    w = Workload("splitk", 384, 384, 1000, 1.5, -0.25, "f32", *orders)
+    inp = make_inputs(w, seed=13, pad=2)
+    full_check(w, inp, pad_d=2, expect_kernel="sgemm_simt<f32")
+
+
+def test_split_k_last_wave_full():
+    w = Workload("splitk_tail", 2560, 2048, 512, 1.5, -0.25, "f32", ROW, ROW, ROW)
+    inp = make_inputs(w, seed=14)
+    full_check(w, inp, pad_d=1, expect_kernel="sgemm_simt<f32")
+
+
+def test_split_k_bf16_fallback_full():
+    # odd leading dimensions keep BF16 on the CUDA-core kernel, which splits K too
+    w = Workload("splitk_bf16", 300, 200, 999, 1.5, -0.25, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=15, pad=2)  # lda = ldb = 1001: not a multiple of 8
+    full_check(w, inp, expect_kernel="sgemm_simt<bf16")
+
+
+@pytest.mark.parametrize("shape", [(384, 384, 1000), (2560, 2048, 512)])
+def test_split_k_is_deterministic_and_exact_on_integers(shape):
+    M, N, K = shape
+    w = Workload("splitk_int", M, N, K, 1.0, 0.0, "f32", dist="int")
+    inp = make_inputs(w, seed=16)
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, D1), ref.astype(np.float32))
+    w = w.with_(dist="uniform")
+    inp = make_inputs(w, seed=17)
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
+
+
 @pytest.mark.parametrize("shape", [(257, 515, 1000), (128, 256, 64), (1, 1, 1), (129, 1, 77),
                                    (1, 300, 513), (640, 512, 8)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
