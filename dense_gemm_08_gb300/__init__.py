@@ -6,8 +6,8 @@ kernels.  Importing this package without the built library raises at the
 first call (there is no CPU fallback).
 
 Same names as the C ABI:
-    gemm_f32, gemm_bf16_f32acc, gemm_status_string, gemm_last_device_status,
-    gemm_last_kernel
+    gemm_f32, gemm_bf16_f32acc, gemm_f32_noalloc, gemm_status_string,
+    gemm_last_device_status, gemm_last_kernel
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
 (torch's current stream).  A non-zero status raises ``GemmError``.
@@ -32,8 +32,8 @@ GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_INTERNAL = 5
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
-EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_status_string", "gemm_last_device_status",
-            "gemm_last_kernel")
+EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f32_noalloc", "gemm_status_string",
+            "gemm_last_device_status", "gemm_last_kernel")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,8 @@ def library() -> ctypes.CDLL:
             lib.gemm_f32.restype = ip
             lib.gemm_bf16_f32acc.argtypes = sig
             lib.gemm_bf16_f32acc.restype = ip
+            lib.gemm_f32_noalloc.argtypes = sig
+            lib.gemm_f32_noalloc.restype = ip
             lib.gemm_status_string.argtypes = [ip]
             lib.gemm_status_string.restype = ctypes.c_char_p
             lib.gemm_last_device_status.argtypes = [vp]
@@ -110,6 +112,15 @@ def gemm_bf16_f32acc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, 
                      order_cd, stream=None, check=True) -> int:
     """BF16-input, FP32-accumulate GEMM (tensor cores when TMA applies; see include/gemm.h)."""
     return _call("gemm_bf16_f32acc", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                 ldc, D, ldd, order_cd, stream, check)
+
+
+def gemm_f32_noalloc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
+                     order_cd, stream=None, check=True) -> int:
+    """gemm_f32 that allocates nothing: its split-K scratch is a fixed 32 MiB
+    array inside the library (for callers that cannot allocate device memory;
+    see include/gemm.h for the limits)."""
+    return _call("gemm_f32_noalloc", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
                  ldc, D, ldd, order_cd, stream, check)
 
 

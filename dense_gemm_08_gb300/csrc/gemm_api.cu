@@ -153,6 +153,31 @@ GEMM_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float a
     return finish(e, name);
 }
 
+GEMM_API gemm_status_t gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                        const float *A, int64_t lda, gemm_order_t order_a,
+                                        const float *B, int64_t ldb, gemm_order_t order_b,
+                                        float beta, const float *C, int64_t ldc, float *D,
+                                        int64_t ldd, gemm_order_t order_cd, cudaStream_t stream) {
+    t_last_kernel = "";
+    gemm_status_t st = validate(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                                ldd, order_cd, sizeof(float));
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if ((st = check_device()) != GEMM_OK) return st;
+    const gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                                      ldc, D, ldd, order_cd);
+    const char *name = "";
+    cudaError_t e;
+    if (K == 0 || alpha == 0.f) {
+        e = gemm::launch_scale_c(p, stream, &name);
+    } else {
+        // the split-tile workspace must fit the fixed array: refuse before any launch
+        if (gemm::simt_f32_scratch_bytes(p) > gemm::kFixedScratchBytes)
+            return GEMM_ERR_INVALID_VALUE;
+        e = gemm::launch_simt_fixed_scratch(p, stream, &name);
+    }
+    return finish(e, name);
+}
+
 GEMM_API const char *gemm_status_string(gemm_status_t status) {
     switch (status) {
         case GEMM_OK: return "success";

@@ -38,6 +38,13 @@ cudaError_t workspace_free(void *ptr, cudaStream_t stream);
 cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name);
 cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **name);
 
+// FP32 CUDA-core path whose split-tile workspace is a fixed file-scope device
+// array of kFixedScratchBytes instead of pool memory (nothing is allocated).
+constexpr size_t kFixedScratchBytes = size_t(32) << 20;
+// Workspace the FP32 CUDA-core path needs for `p` (0 if it splits no tile).
+size_t simt_f32_scratch_bytes(const Problem &p);
+cudaError_t launch_simt_fixed_scratch(const Problem &p, cudaStream_t stream, const char **name);
+
 // Tensor-core (tcgen05) path for BF16 inputs.  Returns cudaErrorNotSupported
 // (without launching) when the operands cannot be described by TMA.
 bool tc_eligible(const Problem &p);

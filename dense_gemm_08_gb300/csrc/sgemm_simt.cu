@@ -25,6 +25,8 @@
 //     outside D ("GEMM on NVIDIA GPUs", section 3 tiled kernel guards).
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace gemm {
@@ -467,8 +469,23 @@ SplitPlan plan_split(const Problem &p, int64_t tiles) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Caller-supplied scratch for the split tiles (see launch_simt_fixed_scratch).
+struct FixedScratch {
+    void *ptr;
+    size_t bytes;
+};
+
+template <typename Cfg>
+size_t split_workspace_bytes(const SplitPlan &plan) {
+    if (plan.tail_tiles == 0) return 0;
+    return align256(static_cast<size_t>(plan.tail_tiles) * plan.max_contrib * Cfg::BM * Cfg::BN *
+                    sizeof(float)) +
+           static_cast<size_t>(plan.tail_tiles) * sizeof(int);
+}
+
 template <typename Cfg, typename T>
-cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name) {
+cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
+                       const FixedScratch *fixed = nullptr) {
     SimtArgs args;
     args.p = p;
     constexpr size_t vbytes = 4 * sizeof(T);
@@ -494,14 +511,23 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name)
         const size_t part_bytes = align256(static_cast<size_t>(plan.tail_tiles) *
                                            plan.max_contrib * Cfg::BM * Cfg::BN * sizeof(float));
         const size_t count_bytes = static_cast<size_t>(plan.tail_tiles) * sizeof(int);
-        cudaError_t e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
-        if (e != cudaSuccess) return e;
-        args.ws_part = static_cast<float *>(ws);
-        args.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
-        e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
-        if (e != cudaSuccess) {
-            workspace_free(ws, stream);
-            return e;
+        if (fixed != nullptr) {
+            // no allocation: the caller's scratch (its size was checked before)
+            if (part_bytes + count_bytes > fixed->bytes) return cudaErrorInvalidValue;
+            args.ws_part = static_cast<float *>(fixed->ptr);
+            args.ws_count = reinterpret_cast<int *>(static_cast<char *>(fixed->ptr) + part_bytes);
+            const cudaError_t e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
+            if (e != cudaSuccess) return e;
+        } else {
+            cudaError_t e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            if (e != cudaSuccess) return e;
+            args.ws_part = static_cast<float *>(ws);
+            args.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
+            e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
+            if (e != cudaSuccess) {
+                workspace_free(ws, stream);
+                return e;
+            }
         }
     }
 
@@ -551,6 +577,65 @@ cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const 
                    : launch_cfg<SmallCfg, float>(p, stream, name);
     return big ? launch_cfg<BigCfg, uint16_t>(p, stream, name)
                : launch_cfg<SmallCfg, uint16_t>(p, stream, name);
+}
+
+// ----------------------------------------------------- fixed-scratch variant
+// For callers that cannot allocate device memory: the split-tile workspace
+// lives in this file-scope array instead of the pool.  Every device that
+// loads the library holds it until the process exits.  In host code the name
+// g_fixed_scratch is only a host-side stand-in for the array, not a device
+// address: the device address is looked up per device with
+// cudaGetSymbolAddress (with that device current) and passed to the kernel.
+namespace {
+__device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+struct FixedScratchAddr {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+FixedScratchAddr g_fixed_addr[kMaxScratchDevices];
+
+// The current device's address of g_fixed_scratch (looked up once per device).
+cudaError_t fixed_scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    FixedScratchAddr &a = g_fixed_addr[dev];
+    std::call_once(a.once, [&a] {
+        void *ptr = nullptr;
+        a.err = cudaGetSymbolAddress(&ptr, g_fixed_scratch);
+        a.ptr = ptr;
+    });
+    *out = a.ptr;
+    return a.err;
+}
+
+template <typename Cfg>
+size_t needed_for(const Problem &p) {
+    const int64_t tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    return split_workspace_bytes<Cfg>(plan_split<Cfg>(p, tiles));
+}
+
+bool use_big(const Problem &p) {
+    const int64_t big_tiles = ((p.M + BigCfg::BM - 1) / BigCfg::BM) *
+                              ((p.N + BigCfg::BN - 1) / BigCfg::BN);
+    return big_tiles >= sm_count();
+}
+}  // namespace
+
+size_t simt_f32_scratch_bytes(const Problem &p) {
+    return use_big(p) ? needed_for<BigCfg>(p) : needed_for<SmallCfg>(p);
+}
+
+cudaError_t launch_simt_fixed_scratch(const Problem &p, cudaStream_t stream, const char **name) {
+    FixedScratch fixed{nullptr, kFixedScratchBytes};
+    const cudaError_t e = fixed_scratch_address(&fixed.ptr);
+    if (e != cudaSuccess) return e;
+    return use_big(p) ? launch_cfg<BigCfg, float>(p, stream, name, &fixed)
+                      : launch_cfg<SmallCfg, float>(p, stream, name, &fixed);
 }
 
 cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **name) {

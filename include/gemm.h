@@ -132,6 +132,41 @@ gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
                                float *D, int64_t ldd, gemm_order_t order_cd,
                                cudaStream_t stream);
 
+/*
+ * gemm_f32_noalloc -- gemm_f32 for callers that cannot allocate device
+ * memory.  The GEMM pages have no counterpart to this entry point; it exists
+ * for code that runs under a device-memory budget fixed in advance, or on
+ * paths where calling the CUDA allocator is not allowed (for example inside
+ * an allocator's own callbacks, or where an allocation could block).
+ *
+ * Arguments, results and accuracy are those of gemm_f32, and it runs the
+ * same kernel with the same work split.  The only difference: when the
+ * kernel splits the K range of its last tiles, the partial sums go to a
+ * fixed 32 MiB array compiled into the library (a file-scope __device__
+ * array that every device holding the library keeps until the process
+ * exits) instead of pool memory, so the call allocates nothing: no
+ * cudaMalloc, no cudaFree, no pool.
+ *
+ * Limits and rules:
+ *   - A problem whose split needs more than 32 MiB of partial sums is
+ *     refused with GEMM_ERR_INVALID_VALUE before anything is enqueued
+ *     (gemm_f32 handles it).  Problems that split no tile need no scratch.
+ *   - The first call on each device looks up that device's address of the
+ *     array (cudaGetSymbolAddress); make that first call before any stream
+ *     capture on that device.
+ *   - All calls on a device share the one array, and it keeps what the last
+ *     call left in it; each call clears the counters it needs.  Calls whose
+ *     work overlaps on the GPU (different streams, no ordering between them)
+ *     race on the array and give wrong results: order them on one stream or
+ *     with events.
+ */
+gemm_status_t gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                               const float *A, int64_t lda, gemm_order_t order_a,
+                               const float *B, int64_t ldb, gemm_order_t order_b,
+                               float beta, const float *C, int64_t ldc,
+                               float *D, int64_t ldd, gemm_order_t order_cd,
+                               cudaStream_t stream);
+
 /* Static English description of a status code; never NULL. */
 const char *gemm_status_string(gemm_status_t status);
 
