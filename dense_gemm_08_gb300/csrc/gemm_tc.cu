@@ -81,8 +81,8 @@ struct TcArgs {
     int64_t ldd;
     int64_t tiles_m, tiles_n, num_kb;
     int a_kmajor, b_kmajor;
-    int vec_c, vec_d;
-    int tma_d;  // D is written through TMA boxes (16-byte aligned base and pitch)
+    int tma_c;  // C is read through TMA boxes (16-byte aligned base and pitch)
+    int tma_d;  // D is written through TMA boxes
     uint64_t timeout_ns;
 };
 
@@ -358,65 +358,54 @@ __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t 
     tn = (t % width) / gsz;
 }
 
-// o[j] = alpha * acc[j] + beta * C[row, c0 + j] for one thread's 32 columns
-// (C read only when use_c; columns past N are left as alpha * acc).
-__device__ __forceinline__ void epilogue_values(const TcArgs &args, const uint32_t (&v)[32],
-                                                const float *crow, int64_t c0, bool use_c,
-                                                bool row_ok, float (&o)[32]) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
-    if (!use_c || !row_ok) return;
-#pragma unroll
-    for (int j4 = 0; j4 < 8; ++j4) {
-        const int64_t col = c0 + j4 * 4;
-        if (col + 3 < args.N && args.vec_c) {
-            // plain load: C may be D itself (in-place update)
-            const float4 c = *reinterpret_cast<const float4 *>(crow + col);
-            o[j4 * 4 + 0] = fmaf(args.beta, c.x, o[j4 * 4 + 0]);
-            o[j4 * 4 + 1] = fmaf(args.beta, c.y, o[j4 * 4 + 1]);
-            o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
-            o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (col + j < args.N) o[j4 * 4 + j] = fmaf(args.beta, crow[col + j], o[j4 * 4 + j]);
-        }
-    }
+// ---------------------------------------------------------- epilogue boxes
+// Each epilogue warp owns two 32 x 32 FP32 boxes in shared memory, laid out
+// with the 128-byte swizzle: element (r, c) sits at byte r * 128 +
+// ((c / 4) ^ (r % 8)) * 16 + (c % 4) * 4.  Thread r reading or writing its own
+// row as eight 16-byte pieces, and the warp reading or writing one row with
+// one element per lane, are both free of bank conflicts; a TMA box with
+// CU_TENSOR_MAP_SWIZZLE_128B uses the same layout.
+__device__ __forceinline__ uint32_t box_offset(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ (r & 7))) << 4) + (c & 3) * 4);
 }
 
-// D[row, c0 .. c0+31] = alpha * acc + beta * C[row, ...] for one thread's row,
-// with 16-byte accesses where the row allows and per-element guards at the edge.
-__device__ __forceinline__ void store_row_chunk(const TcArgs &args, const uint32_t (&v)[32],
-                                                float *drow, const float *crow, int64_t c0,
-                                                bool use_c) {
+// Start copying C[row0 + rr, c0 + lane], rr < 32, into the box with 4-byte
+// asynchronous copies (one coalesced row per instruction; elements outside
+// the matrix are zero-filled) and commit them as one group of this thread.
+__device__ __forceinline__ void box_load_rows_async(uint8_t *box, const TcArgs &a, int64_t row0,
+                                                    int64_t c0, int lane) {
+    const int64_t col = c0 + lane;
+    const bool col_ok = col < a.N;
 #pragma unroll
-    for (int j4 = 0; j4 < 8; ++j4) {
-        const int64_t col = c0 + j4 * 4;
-        float o[4];
+    for (int rr = 0; rr < 32; ++rr) {
+        const int64_t r = row0 + rr;
+        const bool ok = col_ok && r < a.M;
+        const float *src = ok ? a.C + r * a.ldc + col : a.C;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                         smem_addr(box + box_offset(rr, lane))),
+                     "l"(src), "r"(ok ? 4 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's asynchronous-copy groups are pending.
+template <int N>
+__device__ __forceinline__ void async_copy_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The box into D[row0 + rr, c0 + lane], one coalesced row per step, clipped
+// to the matrix.
+__device__ __forceinline__ void box_store_rows(const uint8_t *box, const TcArgs &a, int64_t row0,
+                                               int64_t c0, int lane) {
+    const int64_t col = c0 + lane;
+    const bool col_ok = col < a.N;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = args.alpha * __uint_as_float(v[j4 * 4 + j]);
-        const bool full4 = col + 3 < args.N;
-        if (use_c) {
-            if (full4 && args.vec_c) {
-                // plain load: C may be D itself (in-place update)
-                const float4 c = *reinterpret_cast<const float4 *>(crow + col);
-                o[0] = fmaf(args.beta, c.x, o[0]);
-                o[1] = fmaf(args.beta, c.y, o[1]);
-                o[2] = fmaf(args.beta, c.z, o[2]);
-                o[3] = fmaf(args.beta, c.w, o[3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < args.N) o[j] = fmaf(args.beta, crow[col + j], o[j]);
-            }
-        }
-        if (full4 && args.vec_d) {
-            *reinterpret_cast<float4 *>(drow + col) = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (col + j < args.N) drow[col + j] = o[j];
-        }
+    for (int rr = 0; rr < 32; ++rr) {
+        const int64_t r = row0 + rr;
+        const float d = *reinterpret_cast<const float *>(box + box_offset(rr, lane));
+        if (col_ok && r < a.M) a.D[r * a.ldd + col] = d;
     }
 }
 
@@ -425,6 +414,7 @@ template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_d, const TcArgs args) {
     using C = Cfg<CG>;
     extern __shared__ uint8_t smem_raw[];
@@ -439,7 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
     uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
     uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *cbar = drain + 1;              // [4 x 2]   C box loaded (epilogue warp, box)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cbar + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
@@ -459,6 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_addr(&tempty[b]), 4 * CG);  // one arrival per epilogue warp of the group
         }
         mbar_init(smem_addr(drain), 1);
+        for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&cbar[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -466,6 +458,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b))
                      : "memory");
+        if (args.tma_c)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_c))
+                         : "memory");
         if (args.tma_d)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d))
                          : "memory");
@@ -601,12 +596,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------- epilogue warps 2-5
+        // Per tile, the warp drains its 32 accumulator rows (TMEM lanes) in
+        // 32-column chunks: tcgen05.ld -> D = alpha * acc + beta * C in
+        // registers -> a swizzled 32 x 32 box in shared memory -> one TMA
+        // store (or, when D's pitch cannot be described to TMA, coalesced
+        // row stores).  C arrives in the same box, by TMA one chunk ahead
+        // (or by coalesced row loads), and each thread reads its row from it.
         const int quarter = warp % 4;  // TMEM lanes this warp may access
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool use_c = args.beta != 0.f;
-        uint32_t slab_chunks = 0;  // boxes this warp has staged (selects the staging buffer)
+        const bool tma_c = use_c && args.tma_c;
+        uint8_t *boxes = staging + quarter * 2 * 4096;  // this warp's two boxes
+        const uint32_t cbar0 = smem_addr(&cbar[quarter * 2]);
+        uint32_t nb = 0;      // boxes used so far (box nb & 1 is next)
+        uint32_t cphase = 0;  // bit b: parity of box b's next C arrival
+        bool stop = false;
+        auto issue_c = [&](int b, int64_t c0, int64_t r0) {
+            // lane 0 only; box b is free (no store still reading it)
+            const uint32_t bar = cbar0 + 8 * b;
+            mbar_arrive_expect_tx(bar, 32 * 32 * 4);
+            tma_load_2d<CG>(smem_addr(boxes + b * 4096), &map_c, static_cast<int32_t>(c0),
+                            static_cast<int32_t>(r0), CG == 1 ? bar : map_to_rank(bar, rank));
+        };
         int64_t li = 0;
-        for (int64_t t = group_id; t < n_tiles; t += num_groups, ++li) {
+        for (int64_t t = group_id; t < n_tiles && !stop; t += num_groups, ++li) {
             const int buf = static_cast<int>(li & 1);
             const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
             // lane 0 waits, the warp follows its verdict (keeps the warp converged)
@@ -622,58 +635,110 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             int64_t tm, tn;
             tile_coords(t, args, tm, tn);
-            const int64_t row = tm * C::TILE_M + rank * BM + quarter * 32 + lane;
-            const bool row_ok = row < args.M;
-            float *drow = args.D + row * args.ldd;
-            const float *crow = use_c ? args.C + row * args.ldc : nullptr;
+            const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
+            const int64_t col0 = tn * BN;
+            int n_chunks = 0;  // chunks holding part of D (warp-uniform)
+            if (row0 < args.M) {
+                const int64_t rest = args.N - col0;
+                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+            }
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
-            const int64_t row0 = row - lane;  // first row of this warp's 32-row slab
+            auto release_acc = [&]() {
+                // accumulator rows read: hand the buffer back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t te = smem_addr(&tempty[buf]);
+                    if (CG == 1)
+                        mbar_arrive(te);
+                    else
+                        mbar_arrive_cluster(map_to_rank(te, 0));
+                }
+            };
+            if (use_c && n_chunks > 0) {
+                if (lane == 0) bulk_wait_read<0>();  // the box is not read by an earlier store
+                __syncwarp();
+                if (tma_c) {
+                    if (lane == 0) issue_c(nb & 1, col0, row0);
+                } else {
+                    box_load_rows_async(boxes + (nb & 1) * 4096, args, row0, col0, lane);
+                }
+            }
 #pragma unroll 1
-            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+            for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                const int b = nb & 1;
+                uint8_t *box = boxes + b * 4096;
+                const int64_t c0 = col0 + chunk * 32;
+                const bool more = chunk + 1 < n_chunks;
+                if (use_c && more) {
+                    // C of the next chunk into the other box, one chunk ahead
+                    if (lane == 0) bulk_wait_read<0>();  // the other box's store has read it
+                    __syncwarp();
+                    if (tma_c) {
+                        if (lane == 0) issue_c(b ^ 1, c0 + 32, row0);
+                    } else {
+                        box_load_rows_async(boxes + (b ^ 1) * 4096, args, row0, c0 + 32, lane);
+                    }
+                }
                 uint32_t v[32];
                 __syncwarp();  // tcgen05.ld is warp-collective: converge first
                 tmem_load_32cols(t_acc + chunk * 32, v);
-                if (chunk == BN / 32 - 1) {
-                    // accumulator buffer fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t te = smem_addr(&tempty[buf]);
-                        if (CG == 1)
-                            mbar_arrive(te);
+                if (chunk == n_chunks - 1) release_acc();
+                float o[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                if (use_c) {
+                    if (tma_c) {
+                        int landed = 1;
+                        if (lane == 0)
+                            landed = wait_bounded(cbar0 + 8 * b, (cphase >> b) & 1u, abort_flag,
+                                                  args.timeout_ns);
+                        landed = __shfl_sync(0xffffffffu, landed, 0);
+                        cphase ^= 1u << b;
+                        if (!landed) {
+                            if (lane == 0) raise_abort(abort_flag);
+                            aborted = stop = true;
+                            break;
+                        }
+                    } else {
+                        // this chunk's copies done (the next chunk's may still run)
+                        if (more)
+                            async_copy_wait<1>();
                         else
-                            mbar_arrive_cluster(map_to_rank(te, 0));
+                            async_copy_wait<0>();
+                        __syncwarp();
                     }
-                }
-                const int64_t c0 = tn * BN + chunk * 32;
-                if (c0 >= args.N || row0 >= args.M) continue;  // warp-uniform
-                if (args.tma_d) {
-                    // Stage the 32 x 32 box in shared memory with the 128-byte
-                    // swizzle (16-byte chunk j of row r at position j ^ (r % 8):
-                    // conflict-free) and write it with one TMA store: full
-                    // 128-byte lines instead of 16-byte pieces of 32 rows.
-                    float o[32];
-                    epilogue_values(args, v, crow, c0, use_c, row_ok, o);
-                    const int sb = (slab_chunks++) & 1;
-                    uint8_t *box = staging + (quarter * 2 + sb) * 4096;
-                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
-                    __syncwarp();
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        float4 *dst = reinterpret_cast<float4 *>(box + lane * 128 +
-                                                                 ((j4 ^ (lane & 7)) * 16));
-                        *dst = make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2],
-                                           o[j4 * 4 + 3]);
+                        const float4 c = *reinterpret_cast<const float4 *>(box + box_offset(lane, j4 * 4));
+                        o[j4 * 4 + 0] = fmaf(args.beta, c.x, o[j4 * 4 + 0]);
+                        o[j4 * 4 + 1] = fmaf(args.beta, c.y, o[j4 * 4 + 1]);
+                        o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
+                        o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
                     }
+                    __syncwarp();  // every lane has its C before the box is overwritten
+                } else {
+                    if (lane == 0) bulk_wait_read<1>();  // the store that used this box has read it
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4)
+                    *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
+                        make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
+                if (args.tma_d) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0)
                         tma_store_2d(&map_d, static_cast<int32_t>(c0), static_cast<int32_t>(row0),
                                      smem_addr(box));
-                } else if (row_ok) {
-                    store_row_chunk(args, v, drow, crow, c0, use_c);
+                } else {
+                    __syncwarp();
+                    box_store_rows(box, args, row0, c0, lane);
+                    __syncwarp();
                 }
+                ++nb;
             }
+            if (n_chunks == 0) release_acc();
         }
         if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
         __syncwarp();
@@ -721,6 +786,19 @@ bool encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// 2-D FP32 row-major M x N map with 32 x 32 boxes and the 128-byte swizzle
+// (the epilogue's box layout).
+bool encode_box32_f32(CUtensorMap *map, const void *base, int64_t M, int64_t N, int64_t ld) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 constexpr int kMaxDevices = 64;
@@ -799,26 +877,18 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
         ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
-    // D: FP32 row-major M x N; 32 x 32 boxes with the 128-byte swizzle
-    CUtensorMap map_d;
+    // C and D: FP32 row-major M x N; 32 x 32 boxes with the 128-byte swizzle
+    CUtensorMap map_c, map_d;
     TcArgs a = a0;
-    if (a.tma_d) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ldd) * 4};
-        cuuint32_t box[2] = {32, 32};
-        cuuint32_t estr[2] = {1, 1};
-        const CUresult r = g_encode(&map_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.D, dims, strides,
-                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) a.tma_d = 0;
-    }
-    if (!a.tma_d) map_d = map_a;  // unused placeholder
+    if (a.tma_c && !encode_box32_f32(&map_c, p.C, p.M, p.N, p.ldc)) a.tma_c = 0;
+    if (a.tma_d && !encode_box32_f32(&map_d, p.D, p.M, p.N, p.ldd)) a.tma_d = 0;
+    if (!a.tma_c) map_c = map_a;  // unused placeholders
+    if (!a.tma_d) map_d = map_a;
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr);
-    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, map_d, a);
+    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, map_c, map_d, a);
 }
 
 }  // namespace
@@ -853,9 +923,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.num_kb = (p.K + BK - 1) / BK;
     a.a_kmajor = p.a_kmajor ? 1 : 0;
     a.b_kmajor = p.b_kmajor ? 1 : 0;
-    a.vec_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
-    a.vec_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
-    a.tma_d = a.vec_d;  // TMA needs a 16-byte aligned base and a pitch of whole 16 bytes
+    // TMA needs a 16-byte aligned base and a pitch of whole 16 bytes
+    a.tma_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
+    a.tma_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
