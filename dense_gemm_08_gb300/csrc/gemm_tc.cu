@@ -81,6 +81,14 @@ struct TcArgs {
     int64_t ldd;
     int64_t tiles_m, tiles_n, num_kb;
     int a_kmajor, b_kmajor;
+    // Split-K (fewer tiles than SMs): work item w is tile w / ks, K blocks
+    // [num_kb * s / ks, num_kb * (s + 1) / ks) with s = w % ks.  Each
+    // epilogue warp publishes its 32-row slab of partial sums in ws (one
+    // 4 KiB box per 32 columns), counts itself in ws_count[tile * 4 + warp];
+    // the last of the ks adds the slabs in K order and writes D.
+    int ks;
+    float *ws;
+    int *ws_count;
     int tma_c;  // C is read through TMA boxes (16-byte aligned base and pitch)
     int tma_d;  // D is written through TMA boxes
     uint64_t timeout_ns;
@@ -195,6 +203,25 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t c0,
                  "r"(c0), "r"(c1), "r"(src)
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from shared to global memory (bulk group).
+__device__ __forceinline__ void bulk_copy_to_global(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global to this CTA's shared
+// memory; completion is counted on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_copy_to_shared(uint32_t dst, const void *src, uint32_t bytes,
+                                                    uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // Wait until at most N bulk groups of this thread are still reading shared memory.
@@ -430,7 +457,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
     uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
     uint64_t *cbar = drain + 1;              // [4 x 2]   C box loaded (epilogue warp, box)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cbar + 8);
+    uint64_t *pbar = cbar + 8;               // [4]       split-K pieces loaded (epilogue warp)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pbar + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
@@ -451,6 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(smem_addr(drain), 1);
         for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&cbar[i]), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&pbar[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -473,6 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int64_t n_tiles = args.tiles_m * args.tiles_n;
+    const int64_t n_items = n_tiles * args.ks;
     const uint32_t ring_base = smem_addr(ring);
     bool aborted = false;
 
@@ -483,12 +513,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = group_id; t < n_tiles && ok; t += num_groups) {
+            for (int64_t w = group_id; w < n_items && ok; w += num_groups) {
+                const int64_t t = w / args.ks;
+                const int64_t sp = w % args.ks;
                 int64_t tm, tn;
                 tile_coords(t, args, tm, tn);
                 const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN + rank * C::B_ROWS);
-                for (int64_t kb = 0; kb < args.num_kb; ++kb) {
+                const int64_t kb_end = args.num_kb * (sp + 1) / args.ks;
+                for (int64_t kb = args.num_kb * sp / args.ks; kb < kb_end; ++kb) {
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                       args.timeout_ns)) {
                         raise_abort(abort_flag);
@@ -550,7 +583,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t li = 0;
             bool ok = true;
-            for (int64_t t = group_id; t < n_tiles && ok; t += num_groups, ++li) {
+            for (int64_t w = group_id; w < n_items && ok; w += num_groups, ++li) {
+                const int64_t sp = w % args.ks;
+                const int64_t kb_begin = args.num_kb * sp / args.ks;
+                const int64_t kb_end = args.num_kb * (sp + 1) / args.ks;
                 const int buf = static_cast<int>(li & 1);
                 const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
                 if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
@@ -561,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int64_t kb = 0; kb < args.num_kb; ++kb) {
+                for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag,
                                       args.timeout_ns)) {
                         raise_abort(abort_flag);
@@ -575,7 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = args.a_kmajor ? desc_kmajor(sa, kk) : desc_mnmajor(sa, kk);
                         const uint64_t bd = args.b_kmajor ? desc_kmajor(sb, kk) : desc_mnmajor(sb, kk);
-                        tc_mma<CG>(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma<CG>(d_tmem, ad, bd, idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
                     }
                     tc_commit<CG>(smem_addr(&empty[stage]));  // frees the stage (in both CTAs)
                     if (++stage == C::STAGES) {
@@ -610,6 +646,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t cbar0 = smem_addr(&cbar[quarter * 2]);
         uint32_t nb = 0;      // boxes used so far (box nb & 1 is next)
         uint32_t cphase = 0;  // bit b: parity of box b's next C arrival
+        uint32_t pphase = 0;  // parity of the next split-K piece batch
         bool stop = false;
         auto issue_c = [&](int b, int64_t c0, int64_t r0) {
             // lane 0 only; box b is free (no store still reading it)
@@ -619,7 +656,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             static_cast<int32_t>(r0), CG == 1 ? bar : map_to_rank(bar, rank));
         };
         int64_t li = 0;
-        for (int64_t t = group_id; t < n_tiles && !stop; t += num_groups, ++li) {
+        for (int64_t w = group_id; w < n_items && !stop; w += num_groups, ++li) {
+            const int64_t t = w / args.ks;
+            const int sp = static_cast<int>(w % args.ks);
             const int buf = static_cast<int>(li & 1);
             const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
             // lane 0 waits, the warp follows its verdict (keeps the warp converged)
@@ -655,6 +694,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(map_to_rank(te, 0));
                 }
             };
+            bool split_last = false;  // this warp adds the K pieces of its slab
+            if (args.ks > 1 && n_chunks > 0) {
+                // publish this piece's partial sums: raw accumulator boxes to ws
+#pragma unroll 1
+                for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                    uint8_t *box = boxes + (nb & 1) * 4096;
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_load_32cols(t_acc + chunk * 32, v);
+                    if (lane == 0) bulk_wait_read<1>();  // the copy that used this box has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        *reinterpret_cast<uint4 *>(box + box_offset(lane, j4 * 4)) =
+                            make_uint4(v[j4 * 4 + 0], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        bulk_copy_to_global(args.ws + ((w * 4 + quarter) * 8 + chunk) * 1024,
+                                            smem_addr(box), 4096);
+                    ++nb;
+                }
+                int last = 0;
+                if (lane == 0) {
+                    bulk_wait_all();  // the partial sums are in global memory
+                    __threadfence();
+                    last = atomicAdd(&args.ws_count[t * 4 + quarter], 1) == args.ks - 1;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) {
+                    release_acc();
+                    continue;
+                }
+                __threadfence();  // the other pieces' partial sums are visible
+                split_last = true;
+                if (lane == 0) args.ws_count[t * 4 + quarter] = 0;  // ready for the next call
+            }
             if (use_c && n_chunks > 0) {
                 if (lane == 0) bulk_wait_read<0>();  // the box is not read by an earlier store
                 __syncwarp();
@@ -685,8 +761,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_load_32cols(t_acc + chunk * 32, v);
                 if (chunk == n_chunks - 1) release_acc();
                 float o[32];
+                if (split_last) {
+                    // Sum of the K pieces in K order (the same order on every
+                    // run).  The other pieces' boxes of this chunk come in one
+                    // batch of bulk copies into this warp's quarter of the
+                    // operand ring, idle now: a split CTA has one work item.
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                    if constexpr (CG == 1) {
+                        uint8_t *pieces = ring + quarter * (C::STAGES * C::STAGE_BYTES / 4);
+                        int got = 1;
+                        if (lane == 0) {
+                            const uint32_t bar = smem_addr(&pbar[quarter]);
+                            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(args.ks - 1) * 4096);
+                            for (int s2 = 0, slot = 0; s2 < args.ks; ++s2) {
+                                if (s2 == sp) continue;
+                                bulk_copy_to_shared(
+                                    smem_addr(pieces + slot++ * 4096),
+                                    args.ws + (((t * args.ks + s2) * 4 + quarter) * 8 + chunk) * 1024,
+                                    4096, bar);
+                            }
+                            got = wait_bounded(bar, pphase, abort_flag, args.timeout_ns);
+                        }
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        pphase ^= 1u;
+                        if (!got) {
+                            if (lane == 0) raise_abort(abort_flag);
+                            aborted = stop = true;
+                            break;
+                        }
+                        for (int s2 = 0, slot = 0; s2 < args.ks; ++s2) {
+                            if (s2 == sp) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) o[j] += __uint_as_float(v[j]);
+                            } else {
+                                const uint8_t *part = pieces + slot++ * 4096;
+#pragma unroll
+                                for (int j4 = 0; j4 < 8; ++j4) {
+                                    const float4 pv = *reinterpret_cast<const float4 *>(
+                                        part + box_offset(lane, j4 * 4));
+                                    o[j4 * 4 + 0] += pv.x;
+                                    o[j4 * 4 + 1] += pv.y;
+                                    o[j4 * 4 + 2] += pv.z;
+                                    o[j4 * 4 + 3] += pv.w;
+                                }
+                            }
+                        }
+                        __syncwarp();  // every lane has read the pieces before the next batch
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                }
                 if (use_c) {
                     if (tma_c) {
                         int landed = 1;
@@ -927,6 +1055,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.tma_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
     a.tma_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+    a.ks = 1;
+    a.ws = nullptr;
+    a.ws_count = nullptr;
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
     // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
@@ -936,9 +1067,43 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
         e = launch_variant<2>(p, a, 2 * d->pairs, stream);
     } else {
         const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-        const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
-        *name = "gemm_bf16_tc";
+        // Fewer tiles than SMs: split each tile's K range over ks CTAs
+        // ("GEMM on NVIDIA GPUs", section 5, split-K for short M / N).
+        int64_t ks = 1;
+        if (tiles < d->sms) {
+            ks = d->sms / tiles;
+            if (ks > a.num_kb / 4) ks = a.num_kb / 4;  // at least 4 K blocks per piece
+            // the last piece gathers the other ks - 1 boxes of a chunk in its
+            // warp's quarter of the operand ring
+            const int64_t fit = static_cast<int64_t>(Cfg<1>::STAGES) * Cfg<1>::STAGE_BYTES / 4 / 4096;
+            if (ks > fit + 1) ks = fit + 1;
+            if (ks < 2) ks = 1;
+        }
+        void *ws = nullptr;
+        if (ks > 1) {
+            const size_t part_bytes = static_cast<size_t>(tiles) * ks * 4 * 8 * 4096;
+            const size_t count_bytes = static_cast<size_t>(tiles) * 4 * sizeof(int);
+            e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            if (e != cudaSuccess) return e;
+            a.ws = static_cast<float *>(ws);
+            a.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
+            e = cudaMemsetAsync(a.ws_count, 0, count_bytes, stream);
+            if (e != cudaSuccess) {
+                workspace_free(ws, stream);
+                return e;
+            }
+            a.ks = static_cast<int>(ks);
+            *name = "gemm_bf16_tc<splitk>";
+        } else {
+            *name = "gemm_bf16_tc";
+        }
+        const int64_t items = tiles * ks;
+        const int grid = static_cast<int>(items < d->sms ? items : d->sms);
         e = launch_variant<1>(p, a, grid, stream);
+        if (ws != nullptr) {
+            const cudaError_t ef = workspace_free(ws, stream);
+            if (e == cudaSuccess) e = ef;
+        }
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -111,6 +111,34 @@ def test_cta_pair_variant_all_orders_full(orders):
     full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair>")
 
 
+# Fewer 128 x 256 tiles than SMs and a long K: the tensor-core kernel splits
+# each tile's K range over several CTAs and the last one adds the pieces.
+TC_SPLIT_SHAPE = (300, 600, 2048)
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_tc_split_k_all_orders_full(orders):
+    M, N, K = TC_SPLIT_SHAPE
+    w = Workload("tc_splitk", M, N, K, 1.5, -0.25, "bf16", *orders)
+    inp = make_inputs(w, seed=18, pad=3, ld_multiple=8)
+    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<splitk>")
+
+
+def test_tc_split_k_deterministic_and_exact_on_integers():
+    M, N, K = TC_SPLIT_SHAPE
+    w = Workload("tc_splitk_int", M, N, K, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
+    inp = make_inputs(w, seed=19)
+    D1, _, name = run_gpu(w, inp)
+    assert name == "gemm_bf16_tc<splitk>"
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, D1), ref.astype(np.float32))
+    w = w.with_(dist="normal", alpha=0.5, beta=1.0)
+    inp = make_inputs(w, seed=20)
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
+
+
 def test_cta_pair_variant_small_integers_bit_exact():
     w = Workload("pair_int", 2304, 2560, 1000, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
     inp = make_inputs(w, seed=12)
