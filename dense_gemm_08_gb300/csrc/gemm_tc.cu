@@ -694,9 +694,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(map_to_rank(te, 0));
                 }
             };
-            bool split_last = false;  // this warp adds the K pieces of its slab
+            if constexpr (CG == 1) {
             if (args.ks > 1 && n_chunks > 0) {
-                // publish this piece's partial sums: raw accumulator boxes to ws
+                // ---- split-K: 1) publish this piece's partial sums (raw
+                // accumulator boxes) to ws and count the piece in
+                // ws_count[tile * 4 + warp]
 #pragma unroll 1
                 for (int chunk = 0; chunk < n_chunks; ++chunk) {
                     uint8_t *box = boxes + (nb & 1) * 4096;
@@ -716,20 +718,132 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             smem_addr(box), 4096);
                     ++nb;
                 }
-                int last = 0;
+                release_acc();  // the rest works from the published boxes
+                int ok2 = 1;
                 if (lane == 0) {
                     bulk_wait_all();  // the partial sums are in global memory
                     __threadfence();
-                    last = atomicAdd(&args.ws_count[t * 4 + quarter], 1) == args.ks - 1;
+                    atomicAdd(&args.ws_count[t * 4 + quarter], 1);
+                    // 2) once all ks pieces are published, piece sp reduces
+                    // chunks sp, sp + ks, ... of the slab: the chunks of a
+                    // slab are reduced in parallel by different CTAs (all
+                    // resident: one CTA per SM, cooperative launch)
+                    if (sp < n_chunks) {
+                        const volatile int *cnt = args.ws_count + t * 4 + quarter;
+                        const uint64_t t0 = global_timer();
+                        while (*cnt < args.ks) {
+                            if (*abort_flag || global_timer() - t0 > args.timeout_ns) {
+                                ok2 = 0;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                        __threadfence();
+                    }
                 }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (!last) {
-                    release_acc();
-                    continue;
+                ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+                if (!ok2) {
+                    if (lane == 0) raise_abort(abort_flag);
+                    aborted = stop = true;
+                    break;
                 }
-                __threadfence();  // the other pieces' partial sums are visible
-                split_last = true;
-                if (lane == 0) args.ws_count[t * 4 + quarter] = 0;  // ready for the next call
+                uint8_t *pieces = ring + quarter * (C::STAGES * C::STAGE_BYTES / 4);
+#pragma unroll 1
+                for (int chunk = sp; chunk < n_chunks && !stop; chunk += args.ks) {
+                    const int b = nb & 1;
+                    uint8_t *box = boxes + b * 4096;
+                    const int64_t c0 = col0 + chunk * 32;
+                    // all pieces of this chunk (the operand ring is idle: a split
+                    // CTA has one work item), and C, in flight together
+                    if (lane == 0) {
+                        bulk_wait_read<0>();  // no store still reads this box
+                        const uint32_t bar = smem_addr(&pbar[quarter]);
+                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(args.ks) * 4096);
+                        for (int s2 = 0; s2 < args.ks; ++s2)
+                            bulk_copy_to_shared(
+                                smem_addr(pieces + s2 * 4096),
+                                args.ws + (((t * args.ks + s2) * 4 + quarter) * 8 + chunk) * 1024,
+                                4096, bar);
+                        if (tma_c) issue_c(b, c0, row0);
+                    }
+                    __syncwarp();
+                    if (use_c && !tma_c) box_load_rows_async(box, args, row0, c0, lane);
+                    int got = 1;
+                    if (lane == 0)
+                        got = wait_bounded(smem_addr(&pbar[quarter]), pphase, abort_flag,
+                                           args.timeout_ns);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    pphase ^= 1u;
+                    if (!got) {
+                        if (lane == 0) raise_abort(abort_flag);
+                        aborted = stop = true;
+                        break;
+                    }
+                    // sum of the K pieces in K order (the same order on every run)
+                    float o[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                    for (int s2 = 0; s2 < args.ks; ++s2) {
+                        const uint8_t *part = pieces + s2 * 4096;
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 pv =
+                                *reinterpret_cast<const float4 *>(part + box_offset(lane, j4 * 4));
+                            o[j4 * 4 + 0] += pv.x;
+                            o[j4 * 4 + 1] += pv.y;
+                            o[j4 * 4 + 2] += pv.z;
+                            o[j4 * 4 + 3] += pv.w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
+                    if (use_c) {
+                        if (tma_c) {
+                            int landed = 1;
+                            if (lane == 0)
+                                landed = wait_bounded(cbar0 + 8 * b, (cphase >> b) & 1u,
+                                                      abort_flag, args.timeout_ns);
+                            landed = __shfl_sync(0xffffffffu, landed, 0);
+                            cphase ^= 1u << b;
+                            if (!landed) {
+                                if (lane == 0) raise_abort(abort_flag);
+                                aborted = stop = true;
+                                break;
+                            }
+                        } else {
+                            async_copy_wait<0>();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 c =
+                                *reinterpret_cast<const float4 *>(box + box_offset(lane, j4 * 4));
+                            o[j4 * 4 + 0] = fmaf(args.beta, c.x, o[j4 * 4 + 0]);
+                            o[j4 * 4 + 1] = fmaf(args.beta, c.y, o[j4 * 4 + 1]);
+                            o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
+                            o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
+                        }
+                    }
+                    __syncwarp();  // every lane has read the pieces and C
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
+                            make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
+                    if (args.tma_d) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0)
+                            tma_store_2d(&map_d, static_cast<int32_t>(c0),
+                                         static_cast<int32_t>(row0), smem_addr(box));
+                    } else {
+                        __syncwarp();
+                        box_store_rows(box, args, row0, c0, lane);
+                        __syncwarp();
+                    }
+                    ++nb;
+                }
+                continue;
+            }
             }
             if (use_c && n_chunks > 0) {
                 if (lane == 0) bulk_wait_read<0>();  // the box is not read by an earlier store
@@ -761,57 +875,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_load_32cols(t_acc + chunk * 32, v);
                 if (chunk == n_chunks - 1) release_acc();
                 float o[32];
-                if (split_last) {
-                    // Sum of the K pieces in K order (the same order on every
-                    // run).  The other pieces' boxes of this chunk come in one
-                    // batch of bulk copies into this warp's quarter of the
-                    // operand ring, idle now: a split CTA has one work item.
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
-                    if constexpr (CG == 1) {
-                        uint8_t *pieces = ring + quarter * (C::STAGES * C::STAGE_BYTES / 4);
-                        int got = 1;
-                        if (lane == 0) {
-                            const uint32_t bar = smem_addr(&pbar[quarter]);
-                            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(args.ks - 1) * 4096);
-                            for (int s2 = 0, slot = 0; s2 < args.ks; ++s2) {
-                                if (s2 == sp) continue;
-                                bulk_copy_to_shared(
-                                    smem_addr(pieces + slot++ * 4096),
-                                    args.ws + (((t * args.ks + s2) * 4 + quarter) * 8 + chunk) * 1024,
-                                    4096, bar);
-                            }
-                            got = wait_bounded(bar, pphase, abort_flag, args.timeout_ns);
-                        }
-                        got = __shfl_sync(0xffffffffu, got, 0);
-                        pphase ^= 1u;
-                        if (!got) {
-                            if (lane == 0) raise_abort(abort_flag);
-                            aborted = stop = true;
-                            break;
-                        }
-                        for (int s2 = 0, slot = 0; s2 < args.ks; ++s2) {
-                            if (s2 == sp) {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) o[j] += __uint_as_float(v[j]);
-                            } else {
-                                const uint8_t *part = pieces + slot++ * 4096;
-#pragma unroll
-                                for (int j4 = 0; j4 < 8; ++j4) {
-                                    const float4 pv = *reinterpret_cast<const float4 *>(
-                                        part + box_offset(lane, j4 * 4));
-                                    o[j4 * 4 + 0] += pv.x;
-                                    o[j4 * 4 + 1] += pv.y;
-                                    o[j4 * 4 + 2] += pv.z;
-                                    o[j4 * 4 + 3] += pv.w;
-                                }
-                            }
-                        }
-                        __syncwarp();  // every lane has read the pieces before the next batch
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
-                } else {
+                {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
                 }
@@ -943,19 +1007,28 @@ bool aligned(const void *ptr, size_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) % bytes) == 0;
 }
 
+// cg = 2: clusters of two CTAs.  cg = 1 and `cooperative`: all CTAs are
+// guaranteed to be resident together (the split-K pieces wait for each other).
 cudaLaunchConfig_t launch_config(int grid, int cg, size_t smem, cudaStream_t stream,
-                                 cudaLaunchAttribute *attr) {
+                                 cudaLaunchAttribute *attr, bool cooperative = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    attr->id = cudaLaunchAttributeClusterDimension;
-    attr->val.clusterDim.x = static_cast<unsigned>(cg);
-    attr->val.clusterDim.y = 1;
-    attr->val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 0;
+    if (cg > 1) {
+        attr->id = cudaLaunchAttributeClusterDimension;
+        attr->val.clusterDim.x = static_cast<unsigned>(cg);
+        attr->val.clusterDim.y = 1;
+        attr->val.clusterDim.z = 1;
+        cfg.numAttrs = 1;
+    } else if (cooperative) {
+        attr->id = cudaLaunchAttributeCooperative;
+        attr->val.cooperative = 1;
+        cfg.numAttrs = 1;
+    }
     return cfg;
 }
 
@@ -1015,7 +1088,7 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr);
+    cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr, a.ks > 1);
     return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, map_c, map_d, a);
 }
 
@@ -1073,10 +1146,10 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
         if (tiles < d->sms) {
             ks = d->sms / tiles;
             if (ks > a.num_kb / 4) ks = a.num_kb / 4;  // at least 4 K blocks per piece
-            // the last piece gathers the other ks - 1 boxes of a chunk in its
-            // warp's quarter of the operand ring
+            // a reducing piece gathers the ks boxes of a chunk in its warp's
+            // quarter of the operand ring
             const int64_t fit = static_cast<int64_t>(Cfg<1>::STAGES) * Cfg<1>::STAGE_BYTES / 4 / 4096;
-            if (ks > fit + 1) ks = fit + 1;
+            if (ks > fit) ks = fit;
             if (ks < 2) ks = 1;
         }
         void *ws = nullptr;
