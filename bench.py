@@ -195,7 +195,8 @@ def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None):
         t = t.contiguous()
         if t.dtype.is_floating_point and t.element_size() == 2:
             import torch
-            return t.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+            view = np.float16 if t.dtype == torch.float16 else np.uint16
+            return t.view(torch.int16).numpy().view(view).reshape(-1)
         return t.numpy().reshape(-1)
 
     A, B, C = bits(inp["A"]), bits(inp["B"]), bits(inp["C"])
@@ -245,7 +246,7 @@ def bench_ours(args):
     torch.cuda.set_device(device)
     w = resolve_workload(args)
     inp = make_inputs(w, seed=0)
-    fn = lib.gemm_f32 if w.dtype == "f32" else lib.gemm_bf16_f32acc
+    fn = {"f32": lib.gemm_f32, "bf16": lib.gemm_bf16_f32acc, "f16": lib.gemm_f16_f32acc}[w.dtype]
     in_bytes = 4 if w.dtype == "f32" else 2
 
     A = inp["A"].to(device)
@@ -348,7 +349,7 @@ def bench_ours(args):
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     achieved = w.flops / (ms_per_step * 1e-3) / 1e12
     clk = clock_summary(getattr(clocks, "rows", []))
-    if kname == "gemm_bf16_tc":
+    if kname in ("gemm_bf16_tc", "gemm_f16_tc"):
         timed_s = elapsed_ms * 1e-3
         key = "bf16_tflops_sustained" if timed_s > 1.0 else "bf16_tflops"
         peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
@@ -392,7 +393,7 @@ def bench_ours(args):
         "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
                    "beta": w.beta, "in_dtype": w.dtype, "acc_dtype": "f32", "out_dtype": "f32",
                    "order_a": "row" if w.order_a == 0 else "col",

@@ -6,8 +6,8 @@ kernels.  Importing this package without the built library raises at the
 first call (there is no CPU fallback).
 
 Same names as the C ABI:
-    gemm_f32, gemm_bf16_f32acc, gemm_f32_noalloc, gemm_status_string,
-    gemm_last_device_status, gemm_last_kernel
+    gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_f32_noalloc,
+    gemm_status_string, gemm_last_device_status, gemm_last_kernel
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
 (torch's current stream).  A non-zero status raises ``GemmError``.
@@ -32,8 +32,8 @@ GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_INTERNAL = 5
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
-EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f32_noalloc", "gemm_status_string",
-            "gemm_last_device_status", "gemm_last_kernel")
+EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_noalloc",
+            "gemm_status_string", "gemm_last_device_status", "gemm_last_kernel")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,8 @@ def library() -> ctypes.CDLL:
             lib.gemm_f32.restype = ip
             lib.gemm_bf16_f32acc.argtypes = sig
             lib.gemm_bf16_f32acc.restype = ip
+            lib.gemm_f16_f32acc.argtypes = sig
+            lib.gemm_f16_f32acc.restype = ip
             lib.gemm_f32_noalloc.argtypes = sig
             lib.gemm_f32_noalloc.restype = ip
             lib.gemm_status_string.argtypes = [ip]
@@ -115,6 +117,13 @@ def gemm_bf16_f32acc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, 
                  ldc, D, ldd, order_cd, stream, check)
 
 
+def gemm_f16_f32acc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
+                    order_cd, stream=None, check=True) -> int:
+    """FP16-input, FP32-accumulate GEMM (same kernels as gemm_bf16_f32acc)."""
+    return _call("gemm_f16_f32acc", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                 ldc, D, ldd, order_cd, stream, check)
+
+
 def gemm_f32_noalloc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
                      order_cd, stream=None, check=True) -> int:
     """gemm_f32 that allocates nothing: its split-K scratch is a fixed 32 MiB
@@ -153,8 +162,9 @@ def storage_order(t):
 def gemm(A, B, C=None, alpha=1.0, beta=0.0, out=None, stream=None):
     """D = alpha * A @ B + beta * C for torch CUDA tensors.
 
-    A (M x K) and B (K x N) are float32 (-> gemm_f32) or bfloat16
-    (-> gemm_bf16_f32acc); C and the result are float32 and share one order
+    A (M x K) and B (K x N) are float32 (-> gemm_f32), bfloat16
+    (-> gemm_bf16_f32acc) or float16 (-> gemm_f16_f32acc); C and the result
+    are float32 and share one order
     (``out``'s if given, else C's, else row-major).  Any row- or
     column-major view works (e.g. ``B.t()`` of a contiguous N x K tensor).
     """
@@ -183,9 +193,11 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, out=None, stream=None):
         oc, ldc = storage_order(C)
         if oc != ocd:
             raise ValueError("C and the output must share a storage order")
-    fn = gemm_f32 if A.dtype == torch.float32 else gemm_bf16_f32acc
-    if A.dtype not in (torch.float32, torch.bfloat16):
-        raise TypeError("A and B must be float32 or bfloat16")
+    fns = {torch.float32: gemm_f32, torch.bfloat16: gemm_bf16_f32acc,
+           torch.float16: gemm_f16_f32acc}
+    if A.dtype not in fns:
+        raise TypeError("A and B must be float32, bfloat16 or float16")
+    fn = fns[A.dtype]
     fn(M, N, K, alpha, A, lda, oa, B, ldb, ob, beta, C if beta != 0.0 else None, ldc, out, ldd,
        ocd, stream)
     return out

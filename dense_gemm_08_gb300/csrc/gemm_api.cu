@@ -147,9 +147,32 @@ GEMM_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float a
     if (K == 0 || alpha == 0.f)
         e = gemm::launch_scale_c(p, stream, &name);
     else if (gemm::tc_eligible(p))
-        e = gemm::launch_tc(p, stream, &name);
+        e = gemm::launch_tc(p, gemm::InType::BF16, stream, &name);
     else
         e = gemm::launch_simt(p, gemm::InType::BF16, stream, &name);
+    return finish(e, name);
+}
+
+GEMM_API gemm_status_t gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
+                                       const gemm_f16_t *A, int64_t lda, gemm_order_t order_a,
+                                       const gemm_f16_t *B, int64_t ldb, gemm_order_t order_b,
+                                       float beta, const float *C, int64_t ldc, float *D,
+                                       int64_t ldd, gemm_order_t order_cd, cudaStream_t stream) {
+    t_last_kernel = "";
+    gemm_status_t st = validate(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                                ldd, order_cd, sizeof(gemm_f16_t));
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if ((st = check_device()) != GEMM_OK) return st;
+    const gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
+                                      ldc, D, ldd, order_cd);
+    const char *name = "";
+    cudaError_t e;
+    if (K == 0 || alpha == 0.f)
+        e = gemm::launch_scale_c(p, stream, &name);
+    else if (gemm::tc_eligible(p))
+        e = gemm::launch_tc(p, gemm::InType::F16, stream, &name);
+    else
+        e = gemm::launch_simt(p, gemm::InType::F16, stream, &name);
     return finish(e, name);
 }
 

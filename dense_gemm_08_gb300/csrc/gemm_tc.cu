@@ -1,4 +1,4 @@
-// gemm_tc.cu -- BF16-input, FP32-accumulate GEMM on the sm_103a tensor cores.
+// gemm_tc.cu -- BF16- or FP16-input, FP32-accumulate GEMM on the sm_103a tensor cores.
 //
 // D = alpha * op(A) * op(B) + beta * C, D row-major FP32.
 //
@@ -89,6 +89,7 @@ struct TcArgs {
     int ks;
     float *ws;
     int *ws_count;
+    int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     int tma_c;  // C is read through TMA boxes (16-byte aligned base and pitch)
     int tma_d;  // D is written through TMA boxes
     uint64_t timeout_ns;
@@ -366,11 +367,13 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return smem_desc(tile + kk * UMMA_K * 128, 64 * 128, 1024);
 }
 
-// Instruction descriptor, kind::f16: D FP32 (bits 4-5 = 1), A and B BF16
-// (bits 7-9 = 1, 10-12 = 1), A/B major-ness (bit 15 / 16: 0 = K-major,
-// 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn_major, int b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+// Instruction descriptor, kind::f16: D FP32 (bits 4-5 = 1), A and B format
+// (bits 7-9 and 10-12: 1 = BF16, 0 = FP16), A/B major-ness (bit 15 / 16:
+// 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn_major, int b_mn_major,
+                                                  int ab_format) {
+    return (1u << 4) | (static_cast<uint32_t>(ab_format) << 7) |
+           (static_cast<uint32_t>(ab_format) << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
            (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
 }
@@ -439,7 +442,7 @@ __device__ __forceinline__ void box_store_rows(const uint8_t *box, const TcArgs 
 // ------------------------------------------------------------------- kernel
 template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap map_a,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_d, const TcArgs args) {
@@ -578,7 +581,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && leader) {
-            const uint32_t idesc = make_idesc(C::TILE_M, BN, !args.a_kmajor, !args.b_kmajor);
+            const uint32_t idesc =
+                make_idesc(C::TILE_M, BN, !args.a_kmajor, !args.b_kmajor, args.ab_format);
             int stage = 0;
             uint32_t phase = 0;
             int64_t li = 0;
@@ -964,16 +968,16 @@ bool load_encoder() {
     return g_encode != nullptr;
 }
 
-// 2-D BF16 tensor map: inner dimension `inner` (contiguous), outer `outer`,
+// 2-D 16-bit tensor map: inner dimension `inner` (contiguous), outer `outer`,
 // row pitch ld elements, box = box_inner x box_outer, 128-byte swizzle,
 // out-of-bounds elements read as zero.
-bool encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int64_t ld,
-               uint32_t box_inner, uint32_t box_outer) {
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int64_t inner,
+               int64_t outer, int64_t ld, uint32_t box_inner, uint32_t box_outer) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+    const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1042,18 +1046,18 @@ DeviceInfo *device_info(int dev) {
         d->err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (d->err != cudaSuccess) return;
         d->sms = n > 0 ? n : 1;
-        d->err = cudaFuncSetAttribute(gemm_bf16_tc_kernel<1>,
+        d->err = cudaFuncSetAttribute(gemm_tc_kernel<1>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<1>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
-        d->err = cudaFuncSetAttribute(gemm_bf16_tc_kernel<2>,
+        d->err = cudaFuncSetAttribute(gemm_tc_kernel<2>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<2>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
         cudaLaunchAttribute attr;
         cudaLaunchConfig_t cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2>::SMEM_BYTES, 0, &attr);
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_tc_kernel<2>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2>, &cfg) !=
             cudaSuccess) {
             clusters = 0;
             (void)cudaGetLastError();  // clear it: the pair variant is then not used
@@ -1067,16 +1071,18 @@ template <int CG>
 cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStream_t stream) {
     using C = Cfg<CG>;
     CUtensorMap map_a, map_b;
+    const CUtensorMapDataType dt =
+        a0.ab_format == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     bool ok;
     if (p.a_kmajor)  // A(i, k) at A[i * lda + k]: inner K, outer M; box 64 K x 128 rows
-        ok = encode_2d(&map_a, p.A, p.K, p.M, p.lda, BK, BM);
+        ok = encode_2d(&map_a, dt, p.A, p.K, p.M, p.lda, BK, BM);
     else  // A(i, k) at A[i + k * lda]: inner M, outer K; boxes of 64 M x 64 K
-        ok = encode_2d(&map_a, p.A, p.M, p.K, p.lda, 64, BK);
+        ok = encode_2d(&map_a, dt, p.A, p.M, p.K, p.lda, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
     if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N; box 64 K x B_ROWS
-        ok = encode_2d(&map_b, p.B, p.K, p.N, p.ldb, BK, C::B_ROWS);
+        ok = encode_2d(&map_b, dt, p.B, p.K, p.N, p.ldb, BK, C::B_ROWS);
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
-        ok = encode_2d(&map_b, p.B, p.N, p.K, p.ldb, 64, BK);
+        ok = encode_2d(&map_b, dt, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
     // C and D: FP32 row-major M x N; 32 x 32 boxes with the 128-byte swizzle
     CUtensorMap map_c, map_d;
@@ -1089,7 +1095,7 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr, a.ks > 1);
-    return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<CG>, map_a, map_b, map_c, map_d, a);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG>, map_a, map_b, map_c, map_d, a);
 }
 
 }  // namespace
@@ -1101,7 +1107,9 @@ bool tc_eligible(const Problem &p) {
            p.M < (int64_t(1) << 31) && p.N < (int64_t(1) << 31) && p.K < (int64_t(1) << 31);
 }
 
-cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) {
+cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const char **name) {
+    if (in != InType::BF16 && in != InType::F16) return cudaErrorInvalidValue;
+    const bool bf16 = in == InType::BF16;
     if (!tc_eligible(p)) return cudaErrorNotSupported;
     if (!load_encoder()) return cudaErrorSymbolNotFound;
     int dev = 0;
@@ -1131,12 +1139,13 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
     a.ks = 1;
     a.ws = nullptr;
     a.ws_count = nullptr;
+    a.ab_format = bf16 ? 1 : 0;
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
     // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
     const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
     if (d->pairs > 0 && pair_tiles >= d->pairs) {
-        *name = "gemm_bf16_tc<pair>";
+        *name = bf16 ? "gemm_bf16_tc<pair>" : "gemm_f16_tc<pair>";
         e = launch_variant<2>(p, a, 2 * d->pairs, stream);
     } else {
         const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
@@ -1166,9 +1175,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name) 
                 return e;
             }
             a.ks = static_cast<int>(ks);
-            *name = "gemm_bf16_tc<splitk>";
+            *name = bf16 ? "gemm_bf16_tc<splitk>" : "gemm_f16_tc<splitk>";
         } else {
-            *name = "gemm_bf16_tc";
+            *name = bf16 ? "gemm_bf16_tc" : "gemm_f16_tc";
         }
         const int64_t items = tiles * ks;
         const int grid = static_cast<int>(items < d->sms ? items : d->sms);

@@ -25,7 +25,7 @@ struct Problem {
     int64_t ldd;
 };
 
-enum class InType { F32, BF16 };
+enum class InType { F32, BF16, F16 };
 
 // Temporary device workspace from a library-owned, stream-ordered memory pool
 // (one per device, kept warm between calls): memory handed out on `stream`
@@ -45,10 +45,11 @@ constexpr size_t kFixedScratchBytes = size_t(32) << 20;
 size_t simt_f32_scratch_bytes(const Problem &p);
 cudaError_t launch_simt_fixed_scratch(const Problem &p, cudaStream_t stream, const char **name);
 
-// Tensor-core (tcgen05) path for BF16 inputs.  Returns cudaErrorNotSupported
-// (without launching) when the operands cannot be described by TMA.
+// Tensor-core (tcgen05) path for BF16 or FP16 inputs.  Returns
+// cudaErrorNotSupported (without launching) when the operands cannot be
+// described by TMA.
 bool tc_eligible(const Problem &p);
-cudaError_t launch_tc(const Problem &p, cudaStream_t stream, const char **name);
+cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const char **name);
 // Reads and clears the tensor-core kernel's device status word (after a sync).
 cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status);
 

@@ -1,8 +1,8 @@
 // sgemm_simt.cu -- CUDA-core GEMM: FP32 FMA arithmetic, no tensor cores.
 //
-// Serves gemm_f32 (FP32 inputs) and the BF16 inputs that TMA cannot
-// describe (BF16 values are widened exactly to FP32 when they are staged in
-// shared memory; their products are exact in FP32).
+// Serves gemm_f32 (FP32 inputs) and the BF16 / FP16 inputs that TMA cannot
+// describe (BF16 and FP16 values are widened exactly to FP32 when they are
+// staged in shared memory; their products are exact in FP32).
 //
 // Structure (the CUDA-core steps of "Worklog: optimising GEMM on NVIDIA
 // H100": kernel 2 shared-memory tiling, kernels 3-4 register tiling,
@@ -24,8 +24,10 @@
 //   * tiles past the edge of the matrix load zeros and store nothing
 //     outside D ("GEMM on NVIDIA GPUs", section 3 tiled kernel guards).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -82,6 +84,18 @@ struct Elem<uint16_t> {
         const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
         return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+};
+
+template <>
+struct Elem<__half> {
+    // IEEE binary16 widened exactly to FP32
+    static __device__ __forceinline__ float one(const __half *p) { return __half2float(p[0]); }
+    static __device__ __forceinline__ float4 four(const __half *p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
     }
 };
 
@@ -532,19 +546,26 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
     }
 
     const unsigned grid = static_cast<unsigned>(units < 0x7fffffff ? units : 0x7fffffff);
-    const bool f32 = sizeof(T) == 4;
+    const int kind = sizeof(T) == 4 ? 0 : (std::is_same<T, __half>::value ? 2 : 1);
+    static const char *const names[3][4] = {
+        {"sgemm_simt<f32,A:K,B:K>", "sgemm_simt<f32,A:K,B:N>", "sgemm_simt<f32,A:M,B:K>",
+         "sgemm_simt<f32,A:M,B:N>"},
+        {"sgemm_simt<bf16,A:K,B:K>", "sgemm_simt<bf16,A:K,B:N>", "sgemm_simt<bf16,A:M,B:K>",
+         "sgemm_simt<bf16,A:M,B:N>"},
+        {"sgemm_simt<f16,A:K,B:K>", "sgemm_simt<f16,A:K,B:N>", "sgemm_simt<f16,A:M,B:K>",
+         "sgemm_simt<f16,A:M,B:N>"}};
     if (p.a_kmajor && p.b_kmajor) {
         sgemm_simt_kernel<Cfg, T, true, true><<<grid, Cfg::NT, 0, stream>>>(args);
-        *name = f32 ? "sgemm_simt<f32,A:K,B:K>" : "sgemm_simt<bf16,A:K,B:K>";
+        *name = names[kind][0];
     } else if (p.a_kmajor) {
         sgemm_simt_kernel<Cfg, T, true, false><<<grid, Cfg::NT, 0, stream>>>(args);
-        *name = f32 ? "sgemm_simt<f32,A:K,B:N>" : "sgemm_simt<bf16,A:K,B:N>";
+        *name = names[kind][1];
     } else if (p.b_kmajor) {
         sgemm_simt_kernel<Cfg, T, false, true><<<grid, Cfg::NT, 0, stream>>>(args);
-        *name = f32 ? "sgemm_simt<f32,A:M,B:K>" : "sgemm_simt<bf16,A:M,B:K>";
+        *name = names[kind][2];
     } else {
         sgemm_simt_kernel<Cfg, T, false, false><<<grid, Cfg::NT, 0, stream>>>(args);
-        *name = f32 ? "sgemm_simt<f32,A:M,B:N>" : "sgemm_simt<bf16,A:M,B:N>";
+        *name = names[kind][3];
     }
     cudaError_t e = cudaGetLastError();
     if (ws != nullptr) {
@@ -575,6 +596,9 @@ cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const 
     if (in == InType::F32)
         return big ? launch_cfg<BigCfg, float>(p, stream, name)
                    : launch_cfg<SmallCfg, float>(p, stream, name);
+    if (in == InType::F16)
+        return big ? launch_cfg<BigCfg, __half>(p, stream, name)
+                   : launch_cfg<SmallCfg, __half>(p, stream, name);
     return big ? launch_cfg<BigCfg, uint16_t>(p, stream, name)
                : launch_cfg<SmallCfg, uint16_t>(p, stream, name);
 }

@@ -10,8 +10,8 @@ Recipe (one ``torch.Generator('cpu')`` per call, seeded; draw order A, B, C):
   * "uniform": ``torch.rand * 2 - 1`` in FP32 (uniform on [-1, 1));
     "normal": ``torch.randn * sigma`` in FP32; "int": ``torch.randint(-4, 5)``
     as FP32 (small integers in [-4, 4]);
-  * BF16 operands are the FP32 draws rounded to nearest-even
-    (``Tensor.to(torch.bfloat16)`` on the CPU); C stays FP32;
+  * BF16 / FP16 operands are the FP32 draws rounded to nearest-even
+    (``Tensor.to(torch.bfloat16 / torch.float16)`` on the CPU); C stays FP32;
   * each operand is then laid out in its storage order with leading
     dimension = minimal + ``pad`` (column-major = the transpose stored
     row-major).
@@ -34,7 +34,7 @@ class Workload:
     K: int
     alpha: float
     beta: float
-    dtype: str               # "f32" (gemm_f32) or "bf16" (gemm_bf16_f32acc)
+    dtype: str               # "f32" (gemm_f32), "bf16" (gemm_bf16_f32acc), "f16" (gemm_f16_f32acc)
     order_a: int = ROW
     order_b: int = ROW
     order_cd: int = ROW
@@ -74,6 +74,10 @@ WORKLOADS = {
     # A,B N(0,0.02) -> bf16, C N(0,1) FP32
     "bf16_mlp": Workload("bf16_mlp", 8192, 14336, 4096, 0.5, 1.0, "bf16", ROW, COL, ROW,
                          "normal", 0.02, "normal", 1.0),
+    # FP16-input FP32-accumulate at 8192^3 (the Ada pipeline-depth study's
+    # FP16 -> FP32 workload), A row-major, B column-major, N(0,1) -> FP16
+    "f16_8192": Workload("f16_8192", 8192, 8192, 8192, 1.0, 0.0, "f16", ROW, COL, ROW,
+                         "normal", 1.0),
 }
 for _M, _N, _K in ODD_SHAPES:
     for _dt in ("f32", "bf16"):
@@ -118,9 +122,10 @@ def make_inputs(w: Workload, seed: int = 0, pad: int = 0, ld_multiple: int = 1):
     a = _draw(g, (w.M, w.K), w.dist, w.sigma)
     b = _draw(g, (w.K, w.N), w.dist, w.sigma)
     c = _draw(g, (w.M, w.N), w.c_dist, w.c_sigma) if w.beta != 0 else None
-    if w.dtype == "bf16":
-        a = a.to(torch.bfloat16)
-        b = b.to(torch.bfloat16)
+    if w.dtype in ("bf16", "f16"):
+        t = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        a = a.to(t)
+        b = b.to(t)
     A, lda = _lay_out(a, w.order_a, pad, ld_multiple)
     B, ldb = _lay_out(b, w.order_b, pad, ld_multiple)
     if c is not None:

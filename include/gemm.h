@@ -83,6 +83,9 @@ typedef enum {
 /* One BF16 number as its raw 16-bit pattern (the upper half of an FP32). */
 typedef uint16_t gemm_bf16_t;
 
+/* One IEEE 754 binary16 (FP16) number as its raw 16-bit pattern. */
+typedef uint16_t gemm_f16_t;
+
 /*
  * gemm_f32 -- FP32 inputs, FP32 arithmetic on the CUDA cores (no TF32),
  * FP32 output.  The kernel tiles D into CTA tiles staged through shared
@@ -131,6 +134,24 @@ gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
                                float beta, const float *C, int64_t ldc,
                                float *D, int64_t ldd, gemm_order_t order_cd,
                                cudaStream_t stream);
+
+/*
+ * gemm_f16_f32acc -- FP16 inputs, FP32 accumulation, FP32 C and D.
+ *
+ * The FP16-input, FP32-accumulate GEMM measured in "High-Performance FP16
+ * General Matrix Multiplication on NVIDIA Ada Lovelace via CUTLASS and
+ * WMMA" (methodology and results: FP16 -> FP32 at M = N = K = 8192), on the
+ * same tcgen05 kernels as gemm_bf16_f32acc (kind::f16 with the FP16 operand
+ * format) and the same CUDA-core fallback.  Arguments, contract and
+ * accuracy bound as for gemm_bf16_f32acc; A and B point to binary16 bit
+ * patterns.
+ */
+gemm_status_t gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
+                              const gemm_f16_t *A, int64_t lda, gemm_order_t order_a,
+                              const gemm_f16_t *B, int64_t ldb, gemm_order_t order_b,
+                              float beta, const float *C, int64_t ldc,
+                              float *D, int64_t ldd, gemm_order_t order_cd,
+                              cudaStream_t stream);
 
 /*
  * gemm_f32_noalloc -- gemm_f32 for callers that cannot allocate device

@@ -13,7 +13,8 @@ counting model of "Understanding roofline and tiling through matrix
 multiplication", sections 6.2-6.3 and 10.2, used to pin this oracle.
 
 Storage orders: ``ROW`` stores X(r, q) at X[r*ld + q], ``COL`` at X[r + q*ld].
-BF16 operands are passed as their raw 16-bit patterns (numpy uint16).
+BF16 operands are passed as their raw 16-bit patterns (numpy uint16), FP16
+operands as numpy float16 arrays (read as binary16 bit patterns).
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ ROW = 0
 COL = 1
 IN_F32 = 0
 IN_BF16 = 1
+IN_F16 = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
@@ -85,7 +87,9 @@ def _in_type(a) -> int:
         return IN_F32
     if a.dtype == np.uint16:
         return IN_BF16
-    raise TypeError(f"oracle operands are float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float16:
+        return IN_F16
+    raise TypeError(f"oracle operands are float32, uint16 (bf16 bits) or float16, got {a.dtype}")
 
 
 def _common(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, order_c):

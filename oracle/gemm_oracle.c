@@ -17,11 +17,12 @@
  * storage order of each operand, see below).
  *
  * How:
- *   - Inputs are exactly the bits the GPU receives: FP32 values, or BF16
- *     values (raw 16-bit patterns) widened exactly to double.
+ *   - Inputs are exactly the bits the GPU receives: FP32 values, or BF16 or
+ *     FP16 values (raw 16-bit patterns) widened exactly to double.
  *   - Every product A_ik * B_kj is formed in double.  It is exact: a product
- *     of two FP32 (24-bit significand) or two BF16 (8-bit significand)
- *     numbers needs at most 48 significand bits, and double has 53.
+ *     of two FP32 (24-bit significand), FP16 (11-bit) or BF16 (8-bit)
+ *     numbers needs at most 48 significand bits, and double has 53; FP16
+ *     products span at most 2^-48 .. 2^32, well inside double's range.
  *   - The products are summed over k in increasing order in double, then
  *     d = alpha * s + beta * C_ij in double (IEEE round-to-nearest-even, no
  *     contraction: build with -ffp-contract=off).
@@ -58,6 +59,7 @@
 
 #define ORACLE_IN_F32 0
 #define ORACLE_IN_BF16 1
+#define ORACLE_IN_F16 2
 #define ORACLE_ROW 0
 #define ORACLE_COL 1
 #define ORACLE_MAX_THREADS 256
@@ -85,12 +87,28 @@ static double bf16_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE 754 binary16: sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal numbers are (1024 + fraction) * 2^(exponent - 25), subnormals
+ * fraction * 2^-24; exponent 31 holds infinities and NaNs.  Exact in double. */
+static double f16_to_double(uint16_t bits) {
+    const int sign = bits >> 15, exponent = (bits >> 10) & 0x1f, fraction = bits & 0x3ff;
+    double v;
+    if (exponent == 0)
+        v = ldexp((double)fraction, -24);
+    else if (exponent == 31)
+        v = fraction ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + fraction), exponent - 25);
+    return sign ? -v : v;
+}
+
 static int64_t offset(int order, int64_t ld, int64_t r, int64_t q) {
     return order == ORACLE_ROW ? r * ld + q : r + q * ld;
 }
 
 static double load_in(const problem_t *p, const void *base, int64_t off) {
     if (p->in_type == ORACLE_IN_F32) return (double)((const float *)base)[off];
+    if (p->in_type == ORACLE_IN_F16) return f16_to_double(((const uint16_t *)base)[off]);
     return bf16_to_double(((const uint16_t *)base)[off]);
 }
 
@@ -177,7 +195,8 @@ static int run_parallel(const problem_t *p, int64_t items, void *(*fn)(void *), 
 
 static int check(const problem_t *p) {
     if (p->M < 0 || p->N < 0 || p->K < 0) return -1;
-    if (p->in_type != ORACLE_IN_F32 && p->in_type != ORACLE_IN_BF16) return -1;
+    if (p->in_type != ORACLE_IN_F32 && p->in_type != ORACLE_IN_BF16 && p->in_type != ORACLE_IN_F16)
+        return -1;
     if ((p->order_a | p->order_b | p->order_c) & ~1) return -1;
     if (p->alpha != 0.0 && p->K > 0 && p->M > 0 && p->N > 0 && (!p->A || !p->B)) return -1;
     if (p->beta != 0.0 && p->M > 0 && p->N > 0 && !p->C) return -1;

@@ -14,7 +14,7 @@ from dense_gemm_08_gb300.inputs import COL, ROW, Workload, make_inputs, output_b
 
 F32_REL = 1e-5   # FP32 bound: 1e-5 * S + 1e-6 * |beta C|
 F32_C = 1e-6
-BF16_REL = 4e-3  # BF16 bound: 4e-3 * S + 1e-6
+BF16_REL = 4e-3  # BF16 bound: 4e-3 * S + 1e-6 (also used for FP16 inputs)
 BF16_ABS = 1e-6
 SENTINEL = 1234.5
 
@@ -24,6 +24,8 @@ def np_bits(t: torch.Tensor) -> np.ndarray:
     t = t.contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    if t.dtype == torch.float16:
+        return t.view(torch.int16).numpy().view(np.float16).reshape(-1)
     return t.numpy().reshape(-1)
 
 
@@ -38,7 +40,7 @@ def run_gpu(w: Workload, inp, pad_d: int = 0, device="cuda", stream=None, in_pla
     else:
         Dbuf, ldd = output_buffer(w, pad=pad_d, device=device, fill=SENTINEL,
                                   pad_rows=3 if pad_d else 0)
-    fn = lib.gemm_f32 if w.dtype == "f32" else lib.gemm_bf16_f32acc
+    fn = {"f32": lib.gemm_f32, "bf16": lib.gemm_bf16_f32acc, "f16": lib.gemm_f16_f32acc}[w.dtype]
     fn(w.M, w.N, w.K, w.alpha, A, inp["lda"], w.order_a, B, inp["ldb"], w.order_b, w.beta, C,
        inp["ldc"], Dbuf, ldd, w.order_cd, stream)
     name = lib.gemm_last_kernel()

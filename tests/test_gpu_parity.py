@@ -89,12 +89,12 @@ MODERATE = (300, 600, 200)  # 3 x 3 tensor-core tiles with ragged M, N and K tai
 
 
 @pytest.mark.parametrize("orders", ORDERS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_all_orders_full(dtype, orders):
     M, N, K = MODERATE
     w = Workload(f"mod_{dtype}", M, N, K, 1.5, -0.25, dtype, *orders)
     inp = make_inputs(w, seed=1, pad=3, ld_multiple=8)
-    expect = "gemm_bf16_tc" if dtype == "bf16" else "sgemm_simt<f32"
+    expect = {"f32": "sgemm_simt<f32", "bf16": "gemm_bf16_tc", "f16": "gemm_f16_tc"}[dtype]
     full_check(w, inp, pad_d=5, expect_kernel=expect)
 
 
@@ -137,6 +137,28 @@ def test_tc_split_k_deterministic_and_exact_on_integers():
     D1, _, _ = run_gpu(w, inp)
     D2, _, _ = run_gpu(w, inp)
     assert torch.equal(D1, D2)
+
+
+@pytest.mark.parametrize("orders", [(ROW, COL, ROW), (COL, ROW, COL)])
+def test_f16_pair_and_split_variants_full(orders):
+    for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair>"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk>")]:
+        M, N, K = shape
+        w = Workload("f16var", M, N, K, 1.5, -0.25, "f16", *orders)
+        inp = make_inputs(w, seed=22, pad=5, ld_multiple=8)
+        full_check(w, inp, pad_d=3, expect_kernel=kernel)
+
+
+def test_f16_unaligned_operands_use_cuda_core_path():
+    w = Workload("f16unal", 150, 270, 101, 1.5, -0.25, "f16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=23)  # lda = ldb = 101
+    full_check(w, inp, pad_d=1, expect_kernel="sgemm_simt<f16")
+
+
+def test_f16_8192_sampled():
+    w = WORKLOADS["f16_8192"]
+    inp = make_inputs(w)
+    ratio, kernel = sampled_check(w, inp, rows=(0, w.M // 2 + 3, w.M - 1), cols=(0, w.N - 1))
+    assert kernel == "gemm_f16_tc<pair>"
 
 
 def test_cta_pair_variant_small_integers_bit_exact():
@@ -190,7 +212,7 @@ def test_split_k_is_deterministic_and_exact_on_integers(shape):
 
 @pytest.mark.parametrize("shape", [(257, 515, 1000), (128, 256, 64), (1, 1, 1), (129, 1, 77),
                                    (1, 300, 513), (640, 512, 8)])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_small_integers_bit_exact(dtype, shape):
     M, N, K = shape
     for orders in [(ROW, COL, ROW), (COL, ROW, ROW), (ROW, ROW, COL)]:
@@ -201,7 +223,7 @@ def test_small_integers_bit_exact(dtype, shape):
         assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32)), orders
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_tiny_shapes_brute_force(dtype):
     """Every (M, N, K) in {1..5}^3, every storage order, two (alpha, beta)."""
     for M, N, K in itertools.product(range(1, 6), repeat=3):
@@ -222,9 +244,9 @@ def _dev(t):
     return t.to("cuda") if t is not None else None
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_empty_shapes_are_noops(dtype):
-    fn = lib.gemm_f32 if dtype == "f32" else lib.gemm_bf16_f32acc
+    fn = {"f32": lib.gemm_f32, "bf16": lib.gemm_bf16_f32acc, "f16": lib.gemm_f16_f32acc}[dtype]
     D = torch.full((4, 4), 7.0, device="cuda")
     assert fn(0, 4, 4, 1.0, None, 4, ROW, None, 4, ROW, 0.0, None, 4, D, 4, ROW) == 0
     assert fn(4, 0, 4, 1.0, None, 4, ROW, None, 4, ROW, 0.0, None, 4, D, 4, ROW) == 0
@@ -247,20 +269,20 @@ def test_k_zero_and_alpha_zero_give_beta_c(dtype):
     assert np.array_equal(logical_d(w, Dbuf), (2.0 * inp["C_logical"]).numpy())
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_beta_zero_never_reads_c(dtype):
     w = Workload("b0", 200, 300, 64, 1.0, 0.0, dtype, ROW, COL, ROW)
     inp = make_inputs(w, seed=4, ld_multiple=8)
     A, B = _dev(inp["A"]), _dev(inp["B"])
     Cnan = torch.full((w.M, w.N), float("nan"), device="cuda")
     D = torch.empty((w.M, w.N), device="cuda")
-    fn = lib.gemm_f32 if dtype == "f32" else lib.gemm_bf16_f32acc
+    fn = {"f32": lib.gemm_f32, "bf16": lib.gemm_bf16_f32acc, "f16": lib.gemm_f16_f32acc}[dtype]
     fn(w.M, w.N, w.K, 1.0, A, inp["lda"], ROW, B, inp["ldb"], COL, 0.0, Cnan, w.N, D, w.N, ROW)
     torch.cuda.synchronize()
     assert torch.isfinite(D).all()
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_in_place_c_equals_d(dtype):
     w = Workload("inplace", 260, 520, 130, 0.5, 1.0, dtype, ROW, COL, ROW)
     inp = make_inputs(w, seed=5, ld_multiple=8)

@@ -55,12 +55,16 @@ def bits_to_f32(bits):
 
 def run_oracle(A, B, alpha=1.0, beta=0.0, C=None, orders=(ROW, ROW, ROW), bf16=False, pad=0,
                nthreads=0):
+    """bf16: False (FP32 inputs), True or "bf16" (BF16 inputs), "f16" (FP16 inputs)."""
     A = np.asarray(A, dtype=np.float32)
     B = np.asarray(B, dtype=np.float32)
     M, K = A.shape
     N = B.shape[1]
     oa, ob, oc = orders
-    if bf16:
+    if bf16 == "f16":
+        abuf, lda = store(A.astype(np.float16), oa, pad, np.float16)
+        bbuf, ldb = store(B.astype(np.float16), ob, pad, np.float16)
+    elif bf16:
         abuf, lda = store(bf16_bits(A).reshape(A.shape), oa, pad, np.uint16)
         bbuf, ldb = store(bf16_bits(B).reshape(B.shape), ob, pad, np.uint16)
     else:
@@ -205,13 +209,15 @@ def test_traffic_tables_4096():
 # --------------------------------------------------------------------------
 # 3. Closed forms: identity, permutation, alpha/beta, K = 0
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("bf16", [False, True, "f16"])
 @pytest.mark.parametrize("orders", [(ROW, ROW, ROW), (COL, ROW, COL), (ROW, COL, ROW), (COL, COL, COL)])
 def test_identity_and_permutation(bf16, orders):
     rng = np.random.default_rng(7)
     M, K = 13, 9
     X = rng.uniform(-1, 1, size=(M, K)).astype(np.float32)
-    if bf16:
+    if bf16 == "f16":
+        X = X.astype(np.float16).astype(np.float32)
+    elif bf16:
         X = bits_to_f32(bf16_bits(X)).reshape(M, K)
     D, _ = run_oracle(X, np.eye(K, dtype=np.float32), orders=orders, bf16=bf16)
     assert np.array_equal(D.astype(np.float32), X)
@@ -276,9 +282,9 @@ def test_transpose_identity():
 # --------------------------------------------------------------------------
 # 4. Brute force over tiny shapes and all storage orders
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("bf16", [False, True, "f16"])
 def test_brute_force_tiny(bf16):
-    rng = np.random.default_rng(2024 + bf16)
+    rng = np.random.default_rng(2024 + (2 if bf16 == "f16" else int(bf16)))
     shapes = list(itertools.product(range(1, 6), repeat=3))
     checked = 0
     for (M, N, K) in shapes:
@@ -296,6 +302,23 @@ def test_brute_force_tiny(bf16):
                 assert np.array_equal(S, s_want.astype(np.float64))
                 checked += 1
     assert checked == len(shapes) * 8 * 2
+
+
+def test_f16_widening_matches_every_bit_pattern():
+    """Column of all 65536 binary16 patterns times 1: D holds each value exactly."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16)
+    finite = ~np.isnan(vals)
+    A = np.ascontiguousarray(vals[finite]).reshape(-1, 1)
+    one = np.ones((1, 1), dtype=np.float16)
+    M = A.shape[0]
+    D, _ = oracle.gemm(M, 1, 1, 1.0, A.reshape(-1), 1, ROW, one.reshape(-1), 1, ROW)
+    want = A.reshape(-1).astype(np.float64)  # numpy's binary16 -> double conversion
+    assert np.array_equal(D.reshape(-1), want)
+    # NaN patterns give NaN
+    nan_bits = np.ascontiguousarray(vals[~finite][:64])
+    D, _ = oracle.gemm(nan_bits.shape[0], 1, 1, 1.0, nan_bits, 1, ROW, one.reshape(-1), 1, ROW)
+    assert np.isnan(D).all()
 
 
 def test_rounding_against_exact_sum():
@@ -354,6 +377,8 @@ MUTANTS = {
     "transposed A": ("offset(p->order_a, p->lda, i, k)", "offset(p->order_a, p->lda, k, i)"),
     "column-major formula swapped": ("r * ld + q : r + q * ld", "r + q * ld : r * ld + q"),
     "C read with the wrong order": ("offset(p->order_c, p->ldc, i, j)", "offset(ORACLE_ROW, p->ldc, i, j)"),
+    "FP16 exponent bias off by one": ("exponent - 25", "exponent - 24"),
+    "FP16 implicit bit dropped": ("(double)(1024 + fraction)", "(double)(fraction)"),
 }
 
 
@@ -380,16 +405,17 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         B = small_ints(rng, (K, N))
         C = small_ints(rng, (M, N))
         for orders in itertools.product((ROW, COL), repeat=3):
-            abuf, lda = store(A, orders[0])
-            bbuf, ldb = store(B, orders[1])
-            cbuf, ldc = store(C, orders[2])
-            D = np.zeros((M, N))
-            S = np.zeros((M, N))
-            lib.oracle_gemm(0, M, N, K, 1.5, abuf.ctypes.data, lda, orders[0], bbuf.ctypes.data,
-                            ldb, orders[1], -0.25, cbuf.ctypes.data, ldc, orders[2],
-                            D.ctypes.data, S.ctypes.data, 1)
-            want = exact_reference(A, B, 1.5, -0.25, C)
-            got = [[Fraction(float(D[i, j])) for j in range(N)] for i in range(M)]
-            if got != want:
-                caught = True
+            for in_type, dt in ((0, np.float32), (2, np.float16)):  # FP32 and FP16 inputs
+                abuf, lda = store(A.astype(dt), orders[0], dtype=dt)
+                bbuf, ldb = store(B.astype(dt), orders[1], dtype=dt)
+                cbuf, ldc = store(C, orders[2])
+                D = np.zeros((M, N))
+                S = np.zeros((M, N))
+                lib.oracle_gemm(in_type, M, N, K, 1.5, abuf.ctypes.data, lda, orders[0],
+                                bbuf.ctypes.data, ldb, orders[1], -0.25, cbuf.ctypes.data, ldc,
+                                orders[2], D.ctypes.data, S.ctypes.data, 1)
+                want = exact_reference(A, B, 1.5, -0.25, C)
+                got = [[Fraction(float(D[i, j])) for j in range(N)] for i in range(M)]
+                if got != want:
+                    caught = True
     assert caught, f"mutant '{name}' survived the brute-force pin"
