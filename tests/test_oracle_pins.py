@@ -414,6 +414,9 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
                 lib.oracle_gemm(in_type, M, N, K, 1.5, abuf.ctypes.data, lda, orders[0],
                                 bbuf.ctypes.data, ldb, orders[1], -0.25, cbuf.ctypes.data, ldc,
                                 orders[2], D.ctypes.data, S.ctypes.data, 1)
+                if not np.isfinite(D).all():  # a mutant reading the wrong elements
+                    caught = True
+                    continue
                 want = exact_reference(A, B, 1.5, -0.25, C)
                 got = [[Fraction(float(D[i, j])) for j in range(N)] for i in range(M)]
                 if got != want:
