@@ -63,6 +63,8 @@ def _load():
             lib.oracle_gemm_points.argtypes = [ip, i64, i64, i64, dbl, vp, i64, ip, vp, i64, ip,
                                                dbl, vp, i64, ip, i64, vp, vp, vp, vp, ip]
             lib.oracle_gemm_points.restype = ip
+            lib.oracle_epilogue.argtypes = [i64, i64, vp, vp, ip]
+            lib.oracle_epilogue.restype = ip
             lib.oracle_default_threads.argtypes = []
             lib.oracle_default_threads.restype = ip
             _lib = lib
@@ -133,3 +135,23 @@ def gemm_points(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, 
     if rc != 0:
         raise ValueError("oracle_gemm_points rejected its arguments")
     return D, S
+
+
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_GELU = 2
+
+
+def epilogue(D, bias=None, act=ACT_NONE):
+    """In place on a float64 (M, N) result: D = act(D + bias[None, :]).
+
+    act: ACT_NONE, ACT_RELU (max(x, 0)) or ACT_GELU (tanh form).  Returns D.
+    """
+    assert D.dtype == np.float64 and D.flags.c_contiguous and D.ndim == 2
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        assert bias.shape == (D.shape[1],)
+    rc = _load().oracle_epilogue(D.shape[0], D.shape[1], D.ctypes.data, _ptr(bias), int(act))
+    if rc != 0:
+        raise ValueError("oracle_epilogue rejected its arguments")
+    return D

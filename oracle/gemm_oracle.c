@@ -50,6 +50,7 @@
  * order against an independent loop; tiled == naive at N = 2, 4, 8 with
  * small integers (same page, section 10.3).
  */
+#define _DEFAULT_SOURCE /* M_PI */
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -224,6 +225,32 @@ int oracle_gemm_points(int in_type, int64_t M, int64_t N, int64_t K, double alph
         if (I[t] < 0 || I[t] >= M || J[t] < 0 || J[t] >= N) return -1;
     if (npts == 0) return 0;
     return run_parallel(&p, npts, run_points, I, J, D, S, nthreads);
+}
+
+/*
+ * Fused epilogue, in place on a dense row-major M x N result D (double):
+ * D_ij = act(D_ij + bias_j) -- bias_j added to column j when bias != NULL --
+ * with act = identity (0), ReLU max(x, 0) (1) or GELU in its tanh form
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (2), in double.  This is
+ * the "bias, activation" step of the epilogue in "GEMM on NVIDIA GPUs",
+ * section 4 "Epilogue"; the GELU form is the published tanh approximation
+ * (Hendrycks & Gimpel).  Returns 0, or -1 for an unknown activation.
+ */
+int oracle_epilogue(int64_t M, int64_t N, double *D, const float *bias, int act) {
+    if (act < 0 || act > 2 || M < 0 || N < 0) return -1;
+    const double sqrt_2_over_pi = sqrt(2.0 / M_PI);
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double x = D[i * N + j];
+            if (bias) x += (double)bias[j];
+            if (act == 1)
+                x = x > 0.0 ? x : 0.0;
+            else if (act == 2)
+                x = 0.5 * x * (1.0 + tanh(sqrt_2_over_pi * (x + 0.044715 * x * x * x)));
+            D[i * N + j] = x;
+        }
+    }
+    return 0;
 }
 
 /* Threads the oracle uses for nthreads <= 0 (for reporting). */
