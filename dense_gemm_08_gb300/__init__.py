@@ -6,8 +6,8 @@ kernels.  Importing this package without the built library raises at the
 first call (there is no CPU fallback).
 
 Same names as the C ABI:
-    gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_f32_noalloc,
-    gemm_status_string, gemm_last_device_status, gemm_last_kernel
+    gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_bf16_f32acc_ex,
+    gemm_f32_noalloc, gemm_status_string, gemm_last_device_status, gemm_last_kernel
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
 (torch's current stream).  A non-zero status raises ``GemmError``.
@@ -32,8 +32,20 @@ GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_INTERNAL = 5
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
-EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_f32_noalloc",
-            "gemm_status_string", "gemm_last_device_status", "gemm_last_kernel")
+EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_bf16_f32acc_ex",
+            "gemm_f32_noalloc", "gemm_status_string", "gemm_last_device_status",
+            "gemm_last_kernel")
+
+GEMM_ACT_NONE = 0
+GEMM_ACT_RELU = 1
+GEMM_ACT_GELU = 2
+GEMM_D_F32 = 0
+GEMM_D_BF16 = 1
+
+
+class Epilogue(ctypes.Structure):
+    """gemm_epilogue_t: bias (device pointer or None), activation, d_type."""
+    _fields_ = [("bias", ctypes.c_void_p), ("activation", ctypes.c_int), ("d_type", ctypes.c_int)]
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +75,8 @@ def library() -> ctypes.CDLL:
             lib.gemm_bf16_f32acc.restype = ip
             lib.gemm_f16_f32acc.argtypes = sig
             lib.gemm_f16_f32acc.restype = ip
+            lib.gemm_bf16_f32acc_ex.argtypes = sig[:-1] + [ctypes.POINTER(Epilogue), vp]
+            lib.gemm_bf16_f32acc_ex.restype = ip
             lib.gemm_f32_noalloc.argtypes = sig
             lib.gemm_f32_noalloc.restype = ip
             lib.gemm_status_string.argtypes = [ip]
@@ -122,6 +136,20 @@ def gemm_f16_f32acc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, l
     """FP16-input, FP32-accumulate GEMM (same kernels as gemm_bf16_f32acc)."""
     return _call("gemm_f16_f32acc", M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
                  ldc, D, ldd, order_cd, stream, check)
+
+
+def gemm_bf16_f32acc_ex(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,
+                        order_cd, bias=None, activation=GEMM_ACT_NONE, d_type=GEMM_D_F32,
+                        stream=None, check=True) -> int:
+    """gemm_bf16_f32acc with a fused epilogue: D = act(alpha*AB + beta*C + bias), FP32 or BF16."""
+    ep = Epilogue(_addr(bias), int(activation), int(d_type))
+    st = library().gemm_bf16_f32acc_ex(
+        int(M), int(N), int(K), float(alpha), _addr(A), int(lda), int(order_a), _addr(B),
+        int(ldb), int(order_b), float(beta), _addr(C), int(ldc), _addr(D), int(ldd),
+        int(order_cd), ctypes.byref(ep), _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_bf16_f32acc_ex")
+    return st
 
 
 def gemm_f32_noalloc(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D, ldd,

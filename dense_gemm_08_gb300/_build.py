@@ -20,7 +20,8 @@ LIB_NAME = "libdense_gemm_08_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["gemm_api.cu", "sgemm_simt.cu", "gemm_tc.cu", "workspace.cu"]
-HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(INCLUDE, "gemm.h")]
+HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "epilogue.cuh"),
+           os.path.join(INCLUDE, "gemm.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -35,13 +35,13 @@ int64_t need_ld(gemm_order_t order, int64_t rows, int64_t cols) {
 // Every rule of the contract in gemm.h, checked before any CUDA call.
 gemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                        gemm_order_t oa, const void *B, int64_t ldb, gemm_order_t ob, float beta,
-                       const float *C, int64_t ldc, const float *D, int64_t ldd, gemm_order_t ocd,
-                       size_t in_bytes) {
+                       const float *C, int64_t ldc, const void *D, int64_t ldd, gemm_order_t ocd,
+                       size_t in_bytes, size_t d_bytes = sizeof(float)) {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_VALUE;
     if (!is_order(oa) || !is_order(ob) || !is_order(ocd)) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (D == nullptr || !aligned(D, sizeof(float)) || ldd < need_ld(ocd, M, N))
+    if (D == nullptr || !aligned(D, d_bytes) || ldd < need_ld(ocd, M, N))
         return GEMM_ERR_INVALID_VALUE;
     if (beta != 0.f && (C == nullptr || !aligned(C, sizeof(float)) || ldc < need_ld(ocd, M, N)))
         return GEMM_ERR_INVALID_VALUE;
@@ -173,6 +173,44 @@ GEMM_API gemm_status_t gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, float al
         e = gemm::launch_tc(p, gemm::InType::F16, stream, &name);
     else
         e = gemm::launch_simt(p, gemm::InType::F16, stream, &name);
+    return finish(e, name);
+}
+
+GEMM_API gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                                           const gemm_bf16_t *A, int64_t lda,
+                                           gemm_order_t order_a, const gemm_bf16_t *B,
+                                           int64_t ldb, gemm_order_t order_b, float beta,
+                                           const float *C, int64_t ldc, void *D, int64_t ldd,
+                                           gemm_order_t order_cd, const gemm_epilogue_t *epilogue,
+                                           cudaStream_t stream) {
+    t_last_kernel = "";
+    gemm_epilogue_t ep{nullptr, GEMM_ACT_NONE, GEMM_D_F32};
+    if (epilogue != nullptr) ep = *epilogue;
+    if (ep.activation != GEMM_ACT_NONE && ep.activation != GEMM_ACT_RELU &&
+        ep.activation != GEMM_ACT_GELU)
+        return GEMM_ERR_INVALID_VALUE;
+    if (ep.d_type != GEMM_D_F32 && ep.d_type != GEMM_D_BF16) return GEMM_ERR_INVALID_VALUE;
+    const bool d_bf16 = ep.d_type == GEMM_D_BF16;
+    gemm_status_t st = validate(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc, D,
+                                ldd, order_cd, sizeof(gemm_bf16_t),
+                                d_bf16 ? sizeof(gemm_bf16_t) : sizeof(float));
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if (ep.bias != nullptr && !aligned(ep.bias, sizeof(float))) return GEMM_ERR_INVALID_VALUE;
+    if ((st = check_device()) != GEMM_OK) return st;
+    gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C, ldc,
+                                static_cast<float *>(D), ldd, order_cd);
+    p.bias = ep.bias;
+    p.bias_per_row = order_cd == GEMM_COL_MAJOR;  // columns of D are rows of the stored Dᵀ
+    p.act = static_cast<int>(ep.activation);
+    p.d_bf16 = d_bf16;
+    const char *name = "";
+    cudaError_t e;
+    if (K == 0 || alpha == 0.f)
+        e = gemm::launch_scale_c(p, stream, &name);
+    else if (gemm::tc_eligible(p))
+        e = gemm::launch_tc(p, gemm::InType::BF16, stream, &name);
+    else
+        e = gemm::launch_simt(p, gemm::InType::BF16, stream, &name);
     return finish(e, name);
 }
 

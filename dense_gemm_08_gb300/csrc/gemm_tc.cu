@@ -42,6 +42,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace gemm {
@@ -90,6 +91,11 @@ struct TcArgs {
     float *ws;
     int *ws_count;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
+    // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
+    const float *bias;
+    int bias_per_row;
+    int act;
+    int d_bf16;
     int tma_c;  // C is read through TMA boxes (16-byte aligned base and pitch)
     int tma_d;  // D is written through TMA boxes
     uint64_t timeout_ns;
@@ -439,6 +445,21 @@ __device__ __forceinline__ void box_store_rows(const uint8_t *box, const TcArgs 
     }
 }
 
+// BF16 box (32 rows of 64 bytes, unswizzled) into D[row0 + rr, c0 + lane],
+// one coalesced row per step, clipped to the matrix.
+__device__ __forceinline__ void box_store_rows_bf16(const uint8_t *box, const TcArgs &a,
+                                                    int64_t row0, int64_t c0, int lane) {
+    const int64_t col = c0 + lane;
+    const bool col_ok = col < a.N;
+    uint16_t *d16 = reinterpret_cast<uint16_t *>(a.D);
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+        const int64_t r = row0 + rr;
+        const uint16_t d = *reinterpret_cast<const uint16_t *>(box + rr * 64 + lane * 2);
+        if (col_ok && r < a.M) d16[r * a.ldd + col] = d;
+    }
+}
+
 // ------------------------------------------------------------------- kernel
 template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -659,6 +680,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d<CG>(smem_addr(boxes + b * 4096), &map_c, static_cast<int32_t>(c0),
                             static_cast<int32_t>(r0), CG == 1 ? bar : map_to_rank(bar, rank));
         };
+        // bias, activation, the box, then the box to D (TMA store or rows)
+        auto emit_chunk = [&](float (&o)[32], uint8_t *box, int64_t r0, int64_t c0) {
+            if (args.bias != nullptr) {
+                if (args.bias_per_row) {
+                    const int64_t r = r0 + lane;
+                    const float bv = r < args.M ? args.bias[r] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] += bv;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] += c0 + j < args.N ? args.bias[c0 + j] : 0.f;
+                }
+            }
+            if (args.act != kActNone) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = apply_activation(o[j], args.act);
+            }
+            if (args.d_bf16) {
+                // BF16 box: 32 rows of 64 bytes, unswizzled
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(box + lane * 64 + q8 * 16) =
+                        make_uint4(pack_bf16x2(o[q8 * 8 + 0], o[q8 * 8 + 1]),
+                                   pack_bf16x2(o[q8 * 8 + 2], o[q8 * 8 + 3]),
+                                   pack_bf16x2(o[q8 * 8 + 4], o[q8 * 8 + 5]),
+                                   pack_bf16x2(o[q8 * 8 + 6], o[q8 * 8 + 7]));
+            } else {
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4)
+                    *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
+                        make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
+            }
+            if (args.tma_d) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    tma_store_2d(&map_d, static_cast<int32_t>(c0), static_cast<int32_t>(r0),
+                                 smem_addr(box));
+            } else {
+                __syncwarp();
+                if (args.d_bf16)
+                    box_store_rows_bf16(box, args, r0, c0, lane);
+                else
+                    box_store_rows(box, args, r0, c0, lane);
+                __syncwarp();
+            }
+        };
         int64_t li = 0;
         for (int64_t w = group_id; w < n_items && !stop; w += num_groups, ++li) {
             const int64_t t = w / args.ks;
@@ -829,21 +897,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     __syncwarp();  // every lane has read the pieces and C
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4)
-                        *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
-                            make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
-                    if (args.tma_d) {
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0)
-                            tma_store_2d(&map_d, static_cast<int32_t>(c0),
-                                         static_cast<int32_t>(row0), smem_addr(box));
-                    } else {
-                        __syncwarp();
-                        box_store_rows(box, args, row0, c0, lane);
-                        __syncwarp();
-                    }
+                    emit_chunk(o, box, row0, c0);
                     ++nb;
                 }
                 continue;
@@ -917,21 +971,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) bulk_wait_read<1>();  // the store that used this box has read it
                     __syncwarp();
                 }
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)
-                    *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
-                        make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
-                if (args.tma_d) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0)
-                        tma_store_2d(&map_d, static_cast<int32_t>(c0), static_cast<int32_t>(row0),
-                                     smem_addr(box));
-                } else {
-                    __syncwarp();
-                    box_store_rows(box, args, row0, c0, lane);
-                    __syncwarp();
-                }
+                emit_chunk(o, box, row0, c0);
                 ++nb;
             }
             if (n_chunks == 0) release_acc();
@@ -1088,7 +1128,23 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     CUtensorMap map_c, map_d;
     TcArgs a = a0;
     if (a.tma_c && !encode_box32_f32(&map_c, p.C, p.M, p.N, p.ldc)) a.tma_c = 0;
-    if (a.tma_d && !encode_box32_f32(&map_d, p.D, p.M, p.N, p.ldd)) a.tma_d = 0;
+    if (a.tma_d) {
+        bool ok_d;
+        if (a.d_bf16) {
+            // BF16 D: 32 x 32 boxes of 64-byte rows, unswizzled
+            cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+            cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ldd) * 2};
+            cuuint32_t box[2] = {32, 32};
+            cuuint32_t estr[2] = {1, 1};
+            ok_d = g_encode(&map_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.D, dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+                   CUDA_SUCCESS;
+        } else {
+            ok_d = encode_box32_f32(&map_d, p.D, p.M, p.N, p.ldd);
+        }
+        if (!ok_d) a.tma_d = 0;
+    }
     if (!a.tma_c) map_c = map_a;  // unused placeholders
     if (!a.tma_d) map_d = map_a;
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
@@ -1132,9 +1188,19 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.num_kb = (p.K + BK - 1) / BK;
     a.a_kmajor = p.a_kmajor ? 1 : 0;
     a.b_kmajor = p.b_kmajor ? 1 : 0;
-    // TMA needs a 16-byte aligned base and a pitch of whole 16 bytes
-    a.tma_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0) ? 1 : 0;
-    a.tma_d = (aligned(p.D, 16) && p.ldd % 4 == 0) ? 1 : 0;
+    // TMA needs a 16-byte aligned base and a pitch of whole 16 bytes, and its
+    // stores clip at the matrix edge only in whole 16-byte pieces: C and D go
+    // through TMA boxes only when a row of N elements is whole 16-byte pieces
+    // (otherwise the coalesced row path runs).
+    a.tma_c = (p.beta != 0.f && aligned(p.C, 16) && p.ldc % 4 == 0 && p.N % 4 == 0) ? 1 : 0;
+    a.bias = p.bias;
+    a.bias_per_row = p.bias_per_row ? 1 : 0;
+    a.act = p.act;
+    a.d_bf16 = p.d_bf16 ? 1 : 0;
+    // D rows start on 16 bytes and hold whole 16-byte pieces: ldd and N
+    // multiples of 4 (FP32) or 8 (BF16)
+    const int64_t d_vec = p.d_bf16 ? 8 : 4;
+    a.tma_d = (aligned(p.D, 16) && p.ldd % d_vec == 0 && p.N % d_vec == 0) ? 1 : 0;
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
     a.ks = 1;
     a.ws = nullptr;

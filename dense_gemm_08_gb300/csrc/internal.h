@@ -21,8 +21,14 @@ struct Problem {
     bool b_kmajor;  // B(k, j) at B[k + j * ldb]; else B[k * ldb + j]
     const float *C;  // read only if beta != 0; row-major, ldc
     int64_t ldc;
-    float *D;  // row-major, ldd
+    float *D;  // row-major, ldd (holds BF16 bit patterns when d_bf16)
     int64_t ldd;
+    // Fused epilogue: D = act(alpha * AB + beta * C + bias), stored as FP32 or
+    // BF16.  bias has one value per column of D (per row when bias_per_row).
+    const float *bias = nullptr;
+    bool bias_per_row = false;
+    int act = 0;  // 0 none, 1 ReLU, 2 GELU (tanh form)
+    bool d_bf16 = false;
 };
 
 enum class InType { F32, BF16, F16 };

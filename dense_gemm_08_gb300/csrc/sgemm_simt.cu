@@ -29,6 +29,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace gemm {
@@ -190,7 +191,8 @@ __device__ __forceinline__ void stage_slice(float *__restrict__ xs, const float4
 struct SimtArgs {
     Problem p;
     bool vec_a, vec_b;  // vector global loads of A / B are aligned
-    bool vec_c, vec_d;  // 16-byte accesses of C / D rows are aligned
+    bool vec_c, vec_d;  // 16-byte accesses of C / FP32 D rows are aligned
+    bool vec_d16;       // 8-byte accesses of BF16 D rows are aligned
     int64_t tiles_m, tiles_n;
     // Stream-K tail: tiles [0, full_tiles) are computed whole, one per CTA;
     // the remaining tail_tiles x n_k slice-iterations are dealt out evenly, in
@@ -389,14 +391,16 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             if (threadIdx.x == 0) args.ws_count[slot] = 0;  // ready for the next call
         }
 
-        // epilogue: D = alpha * acc + beta * C
+        // epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
         const bool use_c = p.beta != 0.f;
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int64_t gr = m0 + a_off + (i / 4) * Cfg::LM * 4 + (i % 4);
             if (gr >= p.M) continue;
             float *drow = p.D + gr * p.ldd;
+            uint16_t *drow16 = reinterpret_cast<uint16_t *>(p.D) + gr * p.ldd;
             const float *crow = use_c ? p.C + gr * p.ldc : nullptr;
+            const float row_bias = (p.bias != nullptr && p.bias_per_row) ? p.bias[gr] : 0.f;
 #pragma unroll
             for (int q = 0; q < Cfg::QN; ++q) {
                 const int64_t gc = n0 + b_off + q * Cfg::LN * 4;
@@ -418,7 +422,25 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
                             if (gc + j < p.N) o[j] = fmaf(p.beta, crow[gc + j], o[j]);
                     }
                 }
-                if (full && args.vec_d) {
+                if (p.bias != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        o[j] += p.bias_per_row ? row_bias : (gc + j < p.N ? p.bias[gc + j] : 0.f);
+                }
+                if (p.act != kActNone) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[j] = apply_activation(o[j], p.act);
+                }
+                if (p.d_bf16) {
+                    if (full && args.vec_d16) {
+                        *reinterpret_cast<uint2 *>(drow16 + gc) =
+                            make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (gc + j < p.N) drow16[gc + j] = to_bf16_bits(o[j]);
+                    }
+                } else if (full && args.vec_d) {
                     *reinterpret_cast<float4 *>(drow + gc) = make_float4(o[0], o[1], o[2], o[3]);
                 } else {
 #pragma unroll
@@ -507,6 +529,7 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
     args.vec_b = aligned(p.B, vbytes) && (p.ldb % 4 == 0);
     args.vec_c = p.beta != 0.f && aligned(p.C, 16) && (p.ldc % 4 == 0);
     args.vec_d = aligned(p.D, 16) && (p.ldd % 4 == 0);
+    args.vec_d16 = aligned(p.D, 8) && (p.ldd % 4 == 0);
     args.tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
     args.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
     const int64_t tiles = args.tiles_m * args.tiles_n;
@@ -576,13 +599,18 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
 }
 
 __global__ void scale_c_kernel(const Problem p) {
-    // D = beta * C (beta may be 0: then C is not read and D = 0)
+    // D = act(beta * C + bias) (beta may be 0: then C is not read)
     const int64_t total = p.M * p.N;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t i = e / p.N, j = e % p.N;
-        const float c = p.beta != 0.f ? p.beta * p.C[i * p.ldc + j] : 0.f;
-        p.D[i * p.ldd + j] = c;
+        float c = p.beta != 0.f ? p.beta * p.C[i * p.ldc + j] : 0.f;
+        if (p.bias != nullptr) c += p.bias_per_row ? p.bias[i] : p.bias[j];
+        c = apply_activation(c, p.act);
+        if (p.d_bf16)
+            reinterpret_cast<uint16_t *>(p.D)[i * p.ldd + j] = to_bf16_bits(c);
+        else
+            p.D[i * p.ldd + j] = c;
     }
 }
 

@@ -188,6 +188,46 @@ gemm_status_t gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                float *D, int64_t ldd, gemm_order_t order_cd,
                                cudaStream_t stream);
 
+/*
+ * gemm_bf16_f32acc_ex -- gemm_bf16_f32acc with a fused epilogue:
+ *
+ *     D = act(alpha * op(A) * op(B) + beta * C + bias)
+ *
+ * stored as FP32 or as BF16 (round to nearest even), all in the same kernel
+ * ("GEMM on NVIDIA GPUs", section 4 "Epilogue": alpha, beta, bias,
+ * activation and dtype conversion in the epilogue, no extra round trip;
+ * BF16 output as in "Worklog: optimising GEMM on NVIDIA H100", kernels 7-9).
+ *
+ *   epilogue->bias        N FP32 values, bias[j] added to column j of D, or
+ *                         NULL for none (device pointer, 4-byte aligned)
+ *   epilogue->activation  GEMM_ACT_NONE, GEMM_ACT_RELU (max(x, 0)) or
+ *                         GEMM_ACT_GELU (tanh form:
+ *                         0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))))
+ *   epilogue->d_type      GEMM_D_F32 (D is float) or GEMM_D_BF16 (D holds
+ *                         gemm_bf16_t; its pointer must be 2-byte aligned)
+ *
+ * epilogue == NULL means no bias, no activation, FP32 D (= gemm_bf16_f32acc).
+ * C stays FP32; with a BF16 D, C and D must not overlap.  Everything else
+ * as for gemm_bf16_f32acc.  Accuracy: the bound of gemm_bf16_f32acc on the
+ * pre-activation value, times 1.13 for GELU (its largest slope) plus
+ * 1e-6 |x|, plus 2^-8 |D| for BF16 rounding (half an ulp at 8 significant
+ * bits).
+ */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
+typedef enum { GEMM_D_F32 = 0, GEMM_D_BF16 = 1 } gemm_d_type_t;
+typedef struct {
+    const float *bias;
+    gemm_activation_t activation;
+    gemm_d_type_t d_type;
+} gemm_epilogue_t;
+
+gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                                  const gemm_bf16_t *A, int64_t lda, gemm_order_t order_a,
+                                  const gemm_bf16_t *B, int64_t ldb, gemm_order_t order_b,
+                                  float beta, const float *C, int64_t ldc,
+                                  void *D, int64_t ldd, gemm_order_t order_cd,
+                                  const gemm_epilogue_t *epilogue, cudaStream_t stream);
+
 /* Static English description of a status code; never NULL. */
 const char *gemm_status_string(gemm_status_t status);
 

@@ -311,6 +311,46 @@ def test_bf16_unaligned_operands_use_cuda_core_path():
     assert_within(w, D.cpu().numpy(), ref, S, c_logical(w, inp2))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tensor_core_ignores_operand_padding(dtype):
+    """K (and M, N) not multiples of 8 with 16-byte-multiple leading dimensions:
+    the tensor-core path must read only the matrix, never the padding (NaN here)."""
+    for orders in ORDERS:
+        w = Workload("padnan", 137, 261, 13, 1.5, -0.25, dtype, *orders)
+        inp = make_inputs(w, seed=24, ld_multiple=8)
+        for key in ("A", "B"):
+            logical = inp[key + "_logical"]
+            order = w.order_a if key == "A" else w.order_b
+            store = inp[key]
+            rows, cols = (logical.shape if order == ROW else logical.t().shape)
+            mask = torch.ones_like(store, dtype=torch.bool)
+            mask[:rows, :cols] = False
+            store[mask] = float("nan")
+        C = inp["C"]
+        cmask = torch.ones_like(C, dtype=torch.bool)
+        crow, ccol = (w.M, w.N) if w.order_cd == ROW else (w.N, w.M)
+        cmask[:crow, :ccol] = False
+        C[cmask] = float("nan")
+        Dbuf, _, name = run_gpu(w, inp, pad_d=3)
+        assert name.startswith("gemm_" + dtype + "_tc"), name
+        D = logical_d(w, Dbuf)
+        assert np.isfinite(D).all(), orders
+        ref, S = oracle_full(w, inp)
+        assert_within(w, D, ref, S, c_logical(w, inp), str(orders))
+        check_canary(w, Dbuf)
+
+
+@pytest.mark.parametrize("n", [601, 602, 603, 604, 608])
+def test_tma_store_edges_stay_inside_d(n):
+    """D with a 16-byte-multiple pitch but rows of N elements that are not
+    whole 16-byte pieces: nothing may land past column N."""
+    for dtype, beta in [("bf16", 0.0), ("bf16", -0.25), ("f16", 1.0)]:
+        w = Workload("edge", 200, n, 96, 1.5, beta, dtype, ROW, COL, ROW)
+        inp = make_inputs(w, seed=25, ld_multiple=8)
+        pad = (-n) % 8 + 8  # ldd a multiple of 8 with spare columns
+        full_check(w, inp, pad_d=pad)
+
+
 def test_f32_unaligned_leading_dimensions():
     """Leading dimensions that are not multiples of 4 (scalar loads and stores)."""
     for orders in [(ROW, ROW, ROW), (COL, COL, COL)]:
