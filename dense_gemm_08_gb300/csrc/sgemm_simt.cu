@@ -209,7 +209,11 @@ struct SimtArgs {
 
 constexpr int kGroupM = 8;  // grouped raster: 8 tile-rows share each B column panel
 
-template <typename Cfg, typename T, bool AK, bool BKM>
+// EPI: the fused epilogue (bias, activation, BF16 D) is compiled in.  The
+// plain kernels leave it out: their code stays as small as the alpha/beta
+// epilogue needs, which the instruction cache of the fully unrolled K loop
+// rewards.
+template <typename Cfg, typename T, bool AK, bool BKM, bool EPI>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const SimtArgs args) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, NT = Cfg::NT;
     constexpr int TM = Cfg::TM, TN = Cfg::TN, SA = Cfg::SA, SB = Cfg::SB;
@@ -400,7 +404,8 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             float *drow = p.D + gr * p.ldd;
             uint16_t *drow16 = reinterpret_cast<uint16_t *>(p.D) + gr * p.ldd;
             const float *crow = use_c ? p.C + gr * p.ldc : nullptr;
-            const float row_bias = (p.bias != nullptr && p.bias_per_row) ? p.bias[gr] : 0.f;
+            const float row_bias =
+                (EPI && p.bias != nullptr && p.bias_per_row) ? p.bias[gr] : 0.f;
 #pragma unroll
             for (int q = 0; q < Cfg::QN; ++q) {
                 const int64_t gc = n0 + b_off + q * Cfg::LN * 4;
@@ -422,16 +427,16 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
                             if (gc + j < p.N) o[j] = fmaf(p.beta, crow[gc + j], o[j]);
                     }
                 }
-                if (p.bias != nullptr) {
+                if (EPI && p.bias != nullptr) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         o[j] += p.bias_per_row ? row_bias : (gc + j < p.N ? p.bias[gc + j] : 0.f);
                 }
-                if (p.act != kActNone) {
+                if (EPI && p.act != kActNone) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) o[j] = apply_activation(o[j], p.act);
                 }
-                if (p.d_bf16) {
+                if (EPI && p.d_bf16) {
                     if (full && args.vec_d16) {
                         *reinterpret_cast<uint2 *>(drow16 + gc) =
                             make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
@@ -519,6 +524,22 @@ size_t split_workspace_bytes(const SplitPlan &plan) {
            static_cast<size_t>(plan.tail_tiles) * sizeof(int);
 }
 
+// Only BF16 inputs reach the fused epilogue (gemm_bf16_f32acc_ex); the other
+// input types are built without it.
+template <typename Cfg, typename T, bool AK, bool BKM>
+cudaError_t launch_kernel(bool epi, unsigned grid, const SimtArgs &args, cudaStream_t stream) {
+    if constexpr (std::is_same<T, uint16_t>::value) {
+        if (epi) {
+            sgemm_simt_kernel<Cfg, T, AK, BKM, true><<<grid, Cfg::NT, 0, stream>>>(args);
+            return cudaSuccess;
+        }
+    } else {
+        if (epi) return cudaErrorInvalidValue;
+    }
+    sgemm_simt_kernel<Cfg, T, AK, BKM, false><<<grid, Cfg::NT, 0, stream>>>(args);
+    return cudaSuccess;
+}
+
 template <typename Cfg, typename T>
 cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
                        const FixedScratch *fixed = nullptr) {
@@ -577,20 +598,22 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
          "sgemm_simt<bf16,A:M,B:N>"},
         {"sgemm_simt<f16,A:K,B:K>", "sgemm_simt<f16,A:K,B:N>", "sgemm_simt<f16,A:M,B:K>",
          "sgemm_simt<f16,A:M,B:N>"}};
+    const bool epi = p.bias != nullptr || p.act != kActNone || p.d_bf16;
+    cudaError_t e = cudaSuccess;
     if (p.a_kmajor && p.b_kmajor) {
-        sgemm_simt_kernel<Cfg, T, true, true><<<grid, Cfg::NT, 0, stream>>>(args);
+        e = launch_kernel<Cfg, T, true, true>(epi, grid, args, stream);
         *name = names[kind][0];
     } else if (p.a_kmajor) {
-        sgemm_simt_kernel<Cfg, T, true, false><<<grid, Cfg::NT, 0, stream>>>(args);
+        e = launch_kernel<Cfg, T, true, false>(epi, grid, args, stream);
         *name = names[kind][1];
     } else if (p.b_kmajor) {
-        sgemm_simt_kernel<Cfg, T, false, true><<<grid, Cfg::NT, 0, stream>>>(args);
+        e = launch_kernel<Cfg, T, false, true>(epi, grid, args, stream);
         *name = names[kind][2];
     } else {
-        sgemm_simt_kernel<Cfg, T, false, false><<<grid, Cfg::NT, 0, stream>>>(args);
+        e = launch_kernel<Cfg, T, false, false>(epi, grid, args, stream);
         *name = names[kind][3];
     }
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (ws != nullptr) {
         const cudaError_t ef = workspace_free(ws, stream);
         if (e == cudaSuccess) e = ef;
