@@ -473,6 +473,71 @@ def bench_reference(args):
     }
 
 
+# ------------------------------------------------------------- peak probes
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0  # NVIDIA's GB300 dense BF16 figure (no sparsity)
+
+
+def bench_probe(args):
+    """--probe: the library's peak probes (tensor pipe, FP32 FMA pipe), timed
+    with CUDA events on the launching stream; one JSON line, rank 0 only."""
+    import torch
+    import dense_gemm_08_gb300 as lib
+
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return None
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    reps = max(args.steps, 5)
+
+    def timed(launch):
+        for _ in range(args.warmup):
+            launch()
+        torch.cuda.synchronize(device)
+        times, flops = [], 0.0
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _, flops = launch()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e-3)
+        st = lib.gemm_last_device_status(stream)
+        if st != lib.GEMM_OK:
+            raise RuntimeError(f"probe device status {st}: {lib.gemm_status_string(st)}")
+        med = statistics.median(times)
+        return {"tflops": flops / med / 1e12, "ms": med * 1e3, "flops": flops}
+
+    # each launch about 10 ms at 2 PFLOP/s (tensor) or 80 TFLOP/s (FMA)
+    n_mma = int(0.010 * 2.0e15 / (2 ** 20 * sms))
+    trips = int(0.010 * 80e12 / (2 * 8 * 16 * sms * 8 * 256))
+    peaks, src = load_peaks()
+    with ClockSampler(local) as clk:
+        tc1 = timed(lambda: lib.gemm_probe_tc_bf16(1, n_mma, stream))
+        tc2 = timed(lambda: lib.gemm_probe_tc_bf16(2, n_mma, stream))
+        fma = timed(lambda: lib.gemm_probe_fma_f32(trips, stream))
+    clocks = clock_summary(clk.rows)
+    mhz = clocks["sm_mhz"] if clocks and clocks["sm_mhz"] else None
+    max_mhz = clocks["sm_max_mhz"] if clocks and clocks["sm_max_mhz"] else 2070.0
+    return {
+        "probe": "peaks", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+        "tc_bf16_pair": dict(tc2, n_mma=n_mma, mma="256x256x16 per CTA pair"),
+        "tc_bf16_single": dict(tc1, n_mma=n_mma, mma="128x256x16 per CTA"),
+        "fma_f32": dict(fma, trips=trips),
+        "nominal_bf16_dense_tflops": NOMINAL_BF16_DENSE_TFLOPS,
+        "measured_cublas_bf16_tflops": {"burst": peaks.get("bf16_tflops"),
+                                        "sustained": peaks.get("bf16_tflops_sustained"),
+                                        "source": src},
+        "fp32_formula_tflops": {"at_max_clock": fp32_core_peak_tflops(sms, max_mhz),
+                                "at_run_clock": fp32_core_peak_tflops(sms, mhz) if mhz else None,
+                                "sms": sms},
+        "clocks": clocks,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,9 +551,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--probe", action="store_true",
+                    help="time the library's peak probes instead of a GEMM workload")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
-    line = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if args.probe:
+        line = bench_probe(args)
+    else:
+        line = bench_reference(args) if args.impl == "reference" else bench_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -1,4 +1,5 @@
-"""Python binding of the GB300 GEMM library's C ABI (include/gemm.h).
+"""Python binding of the GB300 GEMM library's C ABI (include/gemm.h and
+include/gemm_probe.h).
 
 Argument marshalling only: every function here forwards to the in-tree
 CUDA library ``libdense_gemm_08_gb300.so``; all arithmetic runs in its
@@ -7,7 +8,8 @@ first call (there is no CPU fallback).
 
 Same names as the C ABI:
     gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_bf16_f32acc_ex,
-    gemm_f32_noalloc, gemm_status_string, gemm_last_device_status, gemm_last_kernel
+    gemm_f32_noalloc, gemm_status_string, gemm_last_device_status, gemm_last_kernel,
+    gemm_probe_tc_bf16, gemm_probe_fma_f32
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
 (torch's current stream).  A non-zero status raises ``GemmError``.
@@ -34,7 +36,7 @@ GEMM_ERR_INTERNAL = 5
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
 EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_bf16_f32acc_ex",
             "gemm_f32_noalloc", "gemm_status_string", "gemm_last_device_status",
-            "gemm_last_kernel")
+            "gemm_last_kernel", "gemm_probe_tc_bf16", "gemm_probe_fma_f32")
 
 GEMM_ACT_NONE = 0
 GEMM_ACT_RELU = 1
@@ -85,6 +87,11 @@ def library() -> ctypes.CDLL:
             lib.gemm_last_device_status.restype = ip
             lib.gemm_last_kernel.argtypes = []
             lib.gemm_last_kernel.restype = ctypes.c_char_p
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.gemm_probe_tc_bf16.argtypes = [ip, i64, dp, vp]
+            lib.gemm_probe_tc_bf16.restype = ip
+            lib.gemm_probe_fma_f32.argtypes = [i64, dp, vp]
+            lib.gemm_probe_fma_f32.restype = ip
             _lib = lib
     return _lib
 
@@ -171,6 +178,25 @@ def gemm_last_device_status(stream=None) -> int:
 
 def gemm_last_kernel() -> str:
     return library().gemm_last_kernel().decode()
+
+
+def gemm_probe_tc_bf16(cta_group, n_mma, stream=None, check=True):
+    """Enqueue the tensor-pipe probe; returns (status, FLOPs of the launch)."""
+    flops = ctypes.c_double(0.0)
+    st = library().gemm_probe_tc_bf16(int(cta_group), int(n_mma), ctypes.byref(flops),
+                                      _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_probe_tc_bf16")
+    return st, flops.value
+
+
+def gemm_probe_fma_f32(trips, stream=None, check=True):
+    """Enqueue the FP32 FMA probe; returns (status, FLOPs of the launch)."""
+    flops = ctypes.c_double(0.0)
+    st = library().gemm_probe_fma_f32(int(trips), ctypes.byref(flops), _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_probe_fma_f32")
+    return st, flops.value
 
 
 # ------------------------------------------------------------ torch helper

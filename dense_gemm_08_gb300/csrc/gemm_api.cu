@@ -11,6 +11,7 @@
 #include <cstdint>
 
 #include "gemm.h"
+#include "gemm_probe.h"
 #include "internal.h"
 
 #define GEMM_API extern "C" __attribute__((visibility("default")))
@@ -258,3 +259,24 @@ GEMM_API gemm_status_t gemm_last_device_status(cudaStream_t stream) {
 }
 
 GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }
+
+// ------------------------------------------------------------ peak probes
+GEMM_API gemm_status_t gemm_probe_tc_bf16(int cta_group, int64_t n_mma, double *flops,
+                                          cudaStream_t stream) {
+    t_last_kernel = "";
+    if ((cta_group != 1 && cta_group != 2) || n_mma < 1 || n_mma > (int64_t(1) << 40) ||
+        flops == nullptr)
+        return GEMM_ERR_INVALID_VALUE;
+    const gemm_status_t dev = check_device();
+    if (dev != GEMM_OK) return dev;
+    return finish(gemm::launch_tc_probe(cta_group, n_mma, stream, flops),
+                  cta_group == 2 ? "tc_probe<pair>" : "tc_probe");
+}
+
+GEMM_API gemm_status_t gemm_probe_fma_f32(int64_t trips, double *flops, cudaStream_t stream) {
+    t_last_kernel = "";
+    if (trips < 1 || trips > (int64_t(1) << 40) || flops == nullptr) return GEMM_ERR_INVALID_VALUE;
+    const gemm_status_t dev = check_device();
+    if (dev != GEMM_OK) return dev;
+    return finish(gemm::launch_fma_probe(trips, stream, flops), "fma_probe");
+}

@@ -992,6 +992,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) tmem_dealloc<CG>(tmem_base);
 }
 
+// -------------------------------------------------------- tensor-pipe probe
+// The tensor pipe with no memory traffic: each CTA (pair) writes one A tile
+// (128 x 64) and one B tile (B_ROWS x 64) of BF16 values into shared memory
+// once, then one lane issues n_mma back-to-back TILE_M x 256 x 16 MMAs into
+// one TMEM accumulator, cycling over the tiles' four 16-deep slices (the
+// MMA stream of the GEMM's mainloop with the loads taken away).
+constexpr int PROBE_THREADS = 128;
+
+template <int CG>
+__global__ void __launch_bounds__(PROBE_THREADS, 1)
+    tc_probe_kernel(int64_t n_mma, uint64_t timeout_ns) {
+    using C = Cfg<CG>;
+    constexpr int kTileBytes = (BM + C::B_ROWS) * BK * 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *done = reinterpret_cast<uint64_t *>(smem + kTileBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    const int warp = threadIdx.x / 32;
+    const uint32_t rank = CG == 1 ? 0u : cluster_rank();
+
+    // operands: BF16 values +-[0.5, 1) with fractions and signs from a
+    // multiplicative hash of the word index, so the multipliers see data
+    // that changes from element to element
+    uint32_t *words = reinterpret_cast<uint32_t *>(smem);
+    for (int i = threadIdx.x; i < kTileBytes / 4; i += PROBE_THREADS) {
+        const uint32_t h = (static_cast<uint32_t>(i) + 0x9E3779B9u * (blockIdx.x + 1u)) * 0x85EBCA6Bu;
+        const uint32_t lo = 0x3F00u | ((h >> 9) & 0x7Fu) | (((h >> 16) & 1u) << 15);
+        const uint32_t hi = 0x3F00u | ((h >> 17) & 0x7Fu) | (((h >> 24) & 1u) << 15);
+        words[i] = lo | (hi << 16);
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(done), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // operands -> tensor pipe
+    if (warp == 0) tmem_alloc<CG>(smem_addr(tmem_slot));
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // both CTAs' operands and barriers are ready
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (threadIdx.x == 0 && rank == 0) {
+        const uint32_t idesc = make_idesc(C::TILE_M, BN, 0, 0, 1);
+        const uint32_t sa = smem_addr(smem), sb = sa + BM * BK * 2;
+        for (int64_t i = 0; i < n_mma; ++i) {
+            const int kk = static_cast<int>(i & (BK / UMMA_K - 1));
+            tc_mma<CG>(tmem_base, desc_kmajor(sa, kk), desc_kmajor(sb, kk), idesc,
+                       i > 0 ? 1u : 0u);
+        }
+        tc_commit<CG>(smem_addr(done));  // CG = 2: arrives on both CTAs' `done`
+    }
+    if (threadIdx.x == 0) {
+        const volatile int never = 0;
+        if (!wait_bounded(smem_addr(done), 0, &never, timeout_ns)) atomicExch(&g_tc_status, 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc<CG>(tmem_base);
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -1254,6 +1318,58 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         }
     }
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_probe(int cta_group, int64_t n_mma, cudaStream_t stream, double *flops) {
+    if ((cta_group != 1 && cta_group != 2) || n_mma < 1) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    DeviceInfo *d = device_info(dev);
+    if (d == nullptr) return cudaErrorInvalidDevice;
+    if (d->err != cudaSuccess) return d->err;
+    // one CTA per SM: the shared memory of the GEMM kernel keeps a second
+    // CTA (and its TMEM allocation) off the SM
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    std::call_once(once[dev], [dev] {
+        attr_err[dev] = cudaFuncSetAttribute(tc_probe_kernel<1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<1>::SMEM_BYTES);
+        if (attr_err[dev] == cudaSuccess)
+            attr_err[dev] = cudaFuncSetAttribute(tc_probe_kernel<2>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<2>::SMEM_BYTES);
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    const int groups = cta_group == 1 ? d->sms : d->pairs;
+    if (groups < 1) return cudaErrorNotSupported;
+    // 1 s per wait, and at least 4x the time the MMAs take at 2 PFLOP/s
+    const double mma_flops = 2.0 * BM * cta_group * BN * UMMA_K;
+    const double est_ns = static_cast<double>(n_mma) * mma_flops * groups / 2.0e6;
+    const uint64_t timeout_ns = static_cast<uint64_t>(est_ns * 4 > 1e9 ? est_ns * 4 : 1e9);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    cfg.gridDim = dim3(static_cast<unsigned>(groups * cta_group), 1, 1);
+    cfg.blockDim = dim3(PROBE_THREADS, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 0;
+    if (cta_group == 2) {
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.numAttrs = 1;
+        cfg.dynamicSmemBytes = Cfg<2>::SMEM_BYTES;
+        e = cudaLaunchKernelEx(&cfg, tc_probe_kernel<2>, n_mma, timeout_ns);
+    } else {
+        cfg.dynamicSmemBytes = Cfg<1>::SMEM_BYTES;
+        e = cudaLaunchKernelEx(&cfg, tc_probe_kernel<1>, n_mma, timeout_ns);
+    }
+    if (e != cudaSuccess) return e;
+    *flops = mma_flops * static_cast<double>(n_mma) * groups;
     return cudaGetLastError();
 }
 

@@ -59,4 +59,13 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
 // Reads and clears the tensor-core kernel's device status word (after a sync).
 cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status);
 
+// Peak probes (no memory traffic).  Each enqueues one kernel on `stream` and
+// stores the FLOPs it performs in *flops.
+//   launch_tc_probe: one CTA per SM (cta_group 1) or one CTA pair per two
+//     SMs (cta_group 2) issuing n_mma back-to-back BF16 tcgen05.mma each.
+//   launch_fma_probe: 8 CTAs of 256 threads per SM, each thread 8 chains of
+//     16 x trips dependent FP32 FMAs.
+cudaError_t launch_tc_probe(int cta_group, int64_t n_mma, cudaStream_t stream, double *flops);
+cudaError_t launch_fma_probe(int64_t trips, cudaStream_t stream, double *flops);
+
 }  // namespace gemm

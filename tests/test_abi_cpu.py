@@ -1,5 +1,5 @@
 """The C-ABI library on a machine without a GPU: it loads, exports exactly
-the entry points include/gemm.h declares, and rejects bad arguments before
+the entry points include/*.h declare, and rejects bad arguments before
 touching CUDA (argument checks need no device)."""
 import ctypes
 import os
@@ -11,15 +11,23 @@ import pytest
 import dense_gemm_08_gb300 as lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gemm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("gemm.h", "gemm_probe.h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
-                       text, flags=re.M)
+    names = []
+    for header in HEADERS:
+        text = open(header).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(
+            r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text,
+            flags=re.M)
     return sorted(set(names))
+
+
+def test_every_header_is_listed():
+    on_disk = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert on_disk == sorted(os.path.basename(h) for h in HEADERS)
 
 
 def test_header_declares_the_abi():
@@ -62,6 +70,18 @@ def test_argument_errors_without_a_device(fn_name):
     # M == 0 is a no-op even with NULL pointers
     assert fn(0, 8, 8, 1.0, None, 8, 0, None, 8, 0, 0.0, None, 8, None, 8, 0, stream=0) == 0
     assert lib.gemm_last_kernel() == ""
+
+
+def test_probe_argument_errors_without_a_device():
+    for cg, n in [(0, 10), (3, 10), (1, 0), (2, -5), (1, 1 << 41)]:
+        st, _ = lib.gemm_probe_tc_bf16(cg, n, stream=0, check=False)
+        assert st == lib.GEMM_ERR_INVALID_VALUE, (cg, n)
+    for trips in [0, -1, 1 << 41]:
+        st, _ = lib.gemm_probe_fma_f32(trips, stream=0, check=False)
+        assert st == lib.GEMM_ERR_INVALID_VALUE, trips
+    # a NULL flops pointer is refused
+    assert lib.library().gemm_probe_fma_f32(10, None, None) == lib.GEMM_ERR_INVALID_VALUE
+    assert lib.library().gemm_probe_tc_bf16(1, 10, None, None) == lib.GEMM_ERR_INVALID_VALUE
 
 
 def test_valid_call_without_a_device_reports_unsupported_device():
