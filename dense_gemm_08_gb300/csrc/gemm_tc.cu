@@ -88,6 +88,14 @@ struct TcArgs {
     // 4 KiB box per 32 columns), counts itself in ws_count[tile * 4 + warp];
     // the last of the ks adds the slabs in K order and writes D.
     int ks;
+    // CTA pairs, last partial round: tiles from tail_first on are split into
+    // tail_ks K ranges, one work item each.  Each piece's epilogue warps
+    // publish their 32-row slab of partial sums in ws and count themselves in
+    // ws_count[((tile - tail_first) * 2 + rank) * 4 + warp]; the last piece
+    // to arrive adds the slabs in K order and writes D (no piece waits for
+    // another).
+    int64_t tail_first;
+    int tail_ks;
     float *ws;
     int *ws_count;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
@@ -384,6 +392,42 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn_major, 
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Work item w of the persistent loop: tile t, piece sp of nsp, K blocks
+// [kb_begin, kb_end).  CG = 1: every tile is split into ks pieces (ks = 1:
+// whole tiles).  CG = 2: whole tiles, then the split tail tiles.
+struct WorkItem {
+    int64_t t, kb_begin, kb_end;
+    int sp, nsp;
+};
+
+template <int CG>
+__device__ __forceinline__ WorkItem work_item(int64_t w, const TcArgs &a) {
+    WorkItem it;
+    if (CG == 1) {
+        it.t = w / a.ks;
+        it.sp = static_cast<int>(w % a.ks);
+        it.nsp = a.ks;
+    } else if (w < a.tail_first) {
+        it.t = w;
+        it.sp = 0;
+        it.nsp = 1;
+    } else {
+        const int64_t r = w - a.tail_first;
+        it.t = a.tail_first + r / a.tail_ks;
+        it.sp = static_cast<int>(r % a.tail_ks);
+        it.nsp = a.tail_ks;
+    }
+    it.kb_begin = a.num_kb * it.sp / it.nsp;
+    it.kb_end = a.num_kb * (it.sp + 1) / it.nsp;
+    return it;
+}
+
+template <int CG>
+__device__ __forceinline__ int64_t work_items(const TcArgs &a) {
+    const int64_t tiles = a.tiles_m * a.tiles_n;
+    return CG == 1 ? tiles * a.ks : a.tail_first + (tiles - a.tail_first) * a.tail_ks;
+}
+
 __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t &tm,
                                             int64_t &tn) {
     const int64_t width = kGroupM * a.tiles_n;
@@ -525,8 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int64_t n_tiles = args.tiles_m * args.tiles_n;
-    const int64_t n_items = n_tiles * args.ks;
+    const int64_t n_items = work_items<CG>(args);
     const uint32_t ring_base = smem_addr(ring);
     bool aborted = false;
 
@@ -538,14 +581,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int64_t w = group_id; w < n_items && ok; w += num_groups) {
-                const int64_t t = w / args.ks;
-                const int64_t sp = w % args.ks;
+                const WorkItem it = work_item<CG>(w, args);
                 int64_t tm, tn;
-                tile_coords(t, args, tm, tn);
+                tile_coords(it.t, args, tm, tn);
                 const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN + rank * C::B_ROWS);
-                const int64_t kb_end = args.num_kb * (sp + 1) / args.ks;
-                for (int64_t kb = args.num_kb * sp / args.ks; kb < kb_end; ++kb) {
+                for (int64_t kb = it.kb_begin; kb < it.kb_end; ++kb) {
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                       args.timeout_ns)) {
                         raise_abort(abort_flag);
@@ -609,9 +650,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int64_t li = 0;
             bool ok = true;
             for (int64_t w = group_id; w < n_items && ok; w += num_groups, ++li) {
-                const int64_t sp = w % args.ks;
-                const int64_t kb_begin = args.num_kb * sp / args.ks;
-                const int64_t kb_end = args.num_kb * (sp + 1) / args.ks;
+                const WorkItem it = work_item<CG>(w, args);
+                const int64_t kb_begin = it.kb_begin;
+                const int64_t kb_end = it.kb_end;
                 const int buf = static_cast<int>(li & 1);
                 const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
                 if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
@@ -729,8 +770,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
         int64_t li = 0;
         for (int64_t w = group_id; w < n_items && !stop; w += num_groups, ++li) {
-            const int64_t t = w / args.ks;
-            const int sp = static_cast<int>(w % args.ks);
+            const WorkItem it = work_item<CG>(w, args);
+            const int64_t t = it.t;
+            const int sp = it.sp;
             const int buf = static_cast<int>(li & 1);
             const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
             // lane 0 waits, the warp follows its verdict (keeps the warp converged)
@@ -766,11 +808,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(map_to_rank(te, 0));
                 }
             };
-            if constexpr (CG == 1) {
-            if (args.ks > 1 && n_chunks > 0) {
-                // ---- split-K: 1) publish this piece's partial sums (raw
-                // accumulator boxes) to ws and count the piece in
-                // ws_count[tile * 4 + warp]
+            if (it.nsp > 1 && n_chunks > 0) {
+                // ---- a split tile.  1) publish this piece's partial sums
+                // (raw accumulator boxes) to ws and count the piece.
+                //   CG = 1: all ks pieces of a tile run at once (cooperative
+                //     launch); once all are counted, piece sp reduces chunks
+                //     sp, sp + ks, ... of the slab -- the chunks of a slab are
+                //     reduced in parallel by different CTAs.
+                //   CG = 2: the last piece to be counted reduces every chunk;
+                //     no piece waits for another.
+                // Either way the pieces are added in K order, so the result
+                // does not depend on which CTA reduces.
+                auto piece_box = [&](int piece, int chunk) -> float * {
+                    const int64_t slot =
+                        CG == 1 ? t * it.nsp + piece
+                                : ((t - args.tail_first) * it.nsp + piece) * 2 + rank;
+                    return args.ws + ((slot * 4 + quarter) * 8 + chunk) * 1024;
+                };
+                int *const counter =
+                    args.ws_count + (CG == 1 ? t * 4 + quarter
+                                             : ((t - args.tail_first) * 2 + rank) * 4 + quarter);
 #pragma unroll 1
                 for (int chunk = 0; chunk < n_chunks; ++chunk) {
                     uint8_t *box = boxes + (nb & 1) * 4096;
@@ -785,57 +842,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             make_uint4(v[j4 * 4 + 0], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0)
-                        bulk_copy_to_global(args.ws + ((w * 4 + quarter) * 8 + chunk) * 1024,
-                                            smem_addr(box), 4096);
+                    if (lane == 0) bulk_copy_to_global(piece_box(sp, chunk), smem_addr(box), 4096);
                     ++nb;
                 }
                 release_acc();  // the rest works from the published boxes
-                int ok2 = 1;
+                int ok2 = 1, reduce = 1;
                 if (lane == 0) {
                     bulk_wait_all();  // the partial sums are in global memory
                     __threadfence();
-                    atomicAdd(&args.ws_count[t * 4 + quarter], 1);
-                    // 2) once all ks pieces are published, piece sp reduces
-                    // chunks sp, sp + ks, ... of the slab: the chunks of a
-                    // slab are reduced in parallel by different CTAs (all
-                    // resident: one CTA per SM, cooperative launch)
-                    if (sp < n_chunks) {
-                        const volatile int *cnt = args.ws_count + t * 4 + quarter;
-                        const uint64_t t0 = global_timer();
-                        while (*cnt < args.ks) {
-                            if (*abort_flag || global_timer() - t0 > args.timeout_ns) {
-                                ok2 = 0;
-                                break;
+                    const int before = atomicAdd(counter, 1);
+                    if (CG == 1) {
+                        // 2) wait until all ks pieces are published (all
+                        // resident: one CTA per SM, cooperative launch)
+                        reduce = sp < n_chunks;
+                        if (reduce) {
+                            const volatile int *cnt = counter;
+                            const uint64_t t0 = global_timer();
+                            while (*cnt < it.nsp) {
+                                if (*abort_flag || global_timer() - t0 > args.timeout_ns) {
+                                    ok2 = 0;
+                                    break;
+                                }
+                                __nanosleep(64);
                             }
-                            __nanosleep(64);
                         }
-                        __threadfence();
+                    } else {
+                        reduce = before == it.nsp - 1;  // the last piece reduces
                     }
+                    if (reduce) __threadfence();
                 }
                 ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+                reduce = __shfl_sync(0xffffffffu, reduce, 0);
                 if (!ok2) {
                     if (lane == 0) raise_abort(abort_flag);
                     aborted = stop = true;
                     break;
                 }
+                if (!reduce) continue;
+                // the operand ring is idle: a split piece is its CTA's last work item
                 uint8_t *pieces = ring + quarter * (C::STAGES * C::STAGE_BYTES / 4);
+                const int first_chunk = CG == 1 ? sp : 0;
+                const int chunk_step = CG == 1 ? it.nsp : 1;
 #pragma unroll 1
-                for (int chunk = sp; chunk < n_chunks && !stop; chunk += args.ks) {
+                for (int chunk = first_chunk; chunk < n_chunks && !stop; chunk += chunk_step) {
                     const int b = nb & 1;
                     uint8_t *box = boxes + b * 4096;
                     const int64_t c0 = col0 + chunk * 32;
-                    // all pieces of this chunk (the operand ring is idle: a split
-                    // CTA has one work item), and C, in flight together
+                    // all pieces of this chunk, and C, in flight together
                     if (lane == 0) {
                         bulk_wait_read<0>();  // no store still reads this box
                         const uint32_t bar = smem_addr(&pbar[quarter]);
-                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(args.ks) * 4096);
-                        for (int s2 = 0; s2 < args.ks; ++s2)
-                            bulk_copy_to_shared(
-                                smem_addr(pieces + s2 * 4096),
-                                args.ws + (((t * args.ks + s2) * 4 + quarter) * 8 + chunk) * 1024,
-                                4096, bar);
+                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(it.nsp) * 4096);
+                        for (int s2 = 0; s2 < it.nsp; ++s2)
+                            bulk_copy_to_shared(smem_addr(pieces + s2 * 4096), piece_box(s2, chunk),
+                                                4096, bar);
                         if (tma_c) issue_c(b, c0, row0);
                     }
                     __syncwarp();
@@ -855,7 +915,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float o[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = 0.f;
-                    for (int s2 = 0; s2 < args.ks; ++s2) {
+                    for (int s2 = 0; s2 < it.nsp; ++s2) {
                         const uint8_t *part = pieces + s2 * 4096;
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
@@ -901,7 +961,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ++nb;
                 }
                 continue;
-            }
             }
             if (use_c && n_chunks > 0) {
                 if (lane == 0) bulk_wait_read<0>();  // the box is not read by an earlier store
@@ -1267,6 +1326,8 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.tma_d = (aligned(p.D, 16) && p.ldd % d_vec == 0 && p.N % d_vec == 0) ? 1 : 0;
     a.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
     a.ks = 1;
+    a.tail_first = 0;
+    a.tail_ks = 1;
     a.ws = nullptr;
     a.ws_count = nullptr;
     a.ab_format = bf16 ? 1 : 0;
@@ -1276,7 +1337,41 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
     if (d->pairs > 0 && pair_tiles >= d->pairs) {
         *name = bf16 ? "gemm_bf16_tc<pair>" : "gemm_f16_tc<pair>";
+        // The tiles of the last, partial round would leave pairs idle: when
+        // they fill at most half of the pairs, split each into tail_ks K
+        // ranges (2 to 4, at least 4 K blocks each) so that round ends sooner.
+        const int64_t groups = d->pairs;
+        const int64_t tail = pair_tiles % groups;
+        int64_t tail_ks = 1;
+        if (tail > 0 && 2 * tail <= groups) {
+            tail_ks = groups / tail;
+            if (tail_ks > 4) tail_ks = 4;
+            if (tail_ks > a.num_kb / 4) tail_ks = a.num_kb / 4;
+            if (tail_ks < 2) tail_ks = 1;
+        }
+        a.tail_first = tail_ks > 1 ? pair_tiles - tail : pair_tiles;
+        a.tail_ks = static_cast<int>(tail_ks);
+        void *ws = nullptr;
+        if (tail_ks > 1) {
+            *name = bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>";
+            // per tail tile and piece: 2 CTAs x 4 warps x 8 boxes of 4 KiB
+            const size_t part_bytes = static_cast<size_t>(tail) * tail_ks * 2 * 4 * 8 * 4096;
+            const size_t count_bytes = static_cast<size_t>(tail) * 2 * 4 * sizeof(int);
+            e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            if (e != cudaSuccess) return e;
+            a.ws = static_cast<float *>(ws);
+            a.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
+            e = cudaMemsetAsync(a.ws_count, 0, count_bytes, stream);
+            if (e != cudaSuccess) {
+                workspace_free(ws, stream);
+                return e;
+            }
+        }
         e = launch_variant<2>(p, a, 2 * d->pairs, stream);
+        if (ws != nullptr) {
+            const cudaError_t ef = workspace_free(ws, stream);
+            if (e == cudaSuccess) e = ef;
+        }
     } else {
         const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
         // Fewer tiles than SMs: split each tile's K range over ks CTAs

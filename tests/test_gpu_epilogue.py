@@ -78,11 +78,11 @@ def test_epilogue_tensor_core_moderate(act, d_type, with_bias):
     check(w, inp, bias, act, d_type, pad_d=8, expect="gemm_bf16_tc")
 
 
-@pytest.mark.parametrize("variant", ["pair", "splitk", "simt", "scale_c", "col_major_d",
-                                     "unaligned_d", "ragged_n"])
+@pytest.mark.parametrize("variant", ["pair", "pair_tail", "splitk", "simt", "scale_c",
+                                     "col_major_d", "unaligned_d", "ragged_n"])
 @pytest.mark.parametrize("d_type", DTYPES)
 def test_epilogue_every_path(variant, d_type):
-    shapes = {"pair": (2500, 2600, 136), "splitk": (300, 600, 2048), "simt": (150, 270, 101),
+    shapes = {"pair": (2500, 2600, 136), "pair_tail": (2000, 3300, 777), "splitk": (300, 600, 2048), "simt": (150, 270, 101),
               "scale_c": (70, 90, 0), "col_major_d": (300, 600, 200), "unaligned_d": (300, 601, 200),
               "ragged_n": (300, 601, 200)}
     M, N, K = shapes[variant]
@@ -90,7 +90,8 @@ def test_epilogue_every_path(variant, d_type):
     w = Workload("epi_" + variant, M, N, K, 1.5, -0.25, "bf16", ROW, COL, order_cd)
     inp = make_inputs(w, seed=33, ld_multiple=1 if variant == "simt" else 8)
     bias = bias_for(w, 34)
-    expect = {"pair": "gemm_bf16_tc<pair>", "splitk": "gemm_bf16_tc<splitk>",
+    expect = {"pair": "gemm_bf16_tc<pair>", "pair_tail": "gemm_bf16_tc<pair",
+              "splitk": "gemm_bf16_tc<splitk>",
               "simt": "sgemm_simt<bf16", "scale_c": "scale_c", "col_major_d": "gemm_bf16_tc",
               "unaligned_d": "gemm_bf16_tc", "ragged_n": "gemm_bf16_tc"}[variant]
     # D rows on 16 bytes (TMA store) except: unaligned_d has an odd ldd (603), and

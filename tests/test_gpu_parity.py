@@ -71,7 +71,7 @@ def test_full_size_config_sampled(name):
     ratio, kernel = sampled_check(w, inp, rows=(0, 1, w.M // 2 + 3, w.M - 1),
                                   cols=(0, w.N // 3 + 1, w.N - 1))
     if w.dtype == "bf16":
-        assert kernel == "gemm_bf16_tc<pair>"
+        assert kernel.startswith("gemm_bf16_tc<pair")
 
 
 @pytest.mark.parametrize("name", sorted(k for k in WORKLOADS if k.startswith("odd_")))
@@ -158,16 +158,55 @@ def test_f16_8192_sampled():
     w = WORKLOADS["f16_8192"]
     inp = make_inputs(w)
     ratio, kernel = sampled_check(w, inp, rows=(0, w.M // 2 + 3, w.M - 1), cols=(0, w.N - 1))
-    assert kernel == "gemm_f16_tc<pair>"
+    assert kernel.startswith("gemm_f16_tc<pair")
 
 
 def test_cta_pair_variant_small_integers_bit_exact():
     w = Workload("pair_int", 2304, 2560, 1000, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
     inp = make_inputs(w, seed=12)
     Dbuf, _, name = run_gpu(w, inp)
-    assert name == "gemm_bf16_tc<pair>"
+    assert name.startswith("gemm_bf16_tc<pair")
     ref, _ = oracle_full(w, inp)
     assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
+
+
+# The CTA-pair kernel's last round: with 76 resident pairs these shapes leave
+# 28, 20 and 14 tiles for it, which are split into 2, 3 and 4 K ranges; the
+# last piece to finish adds them.  Ragged M, N and K in the first.
+TAIL_SHAPES = [(2000, 3300, 777), (2048, 3072, 768), (2304, 2560, 1024)]
+
+
+def _pairs_resident():
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_cta_pair_split_tail_all_orders_full(orders):
+    M, N, K = TAIL_SHAPES[0]
+    w = Workload("pair_tail", M, N, K, 1.5, -0.25, "bf16", *orders)
+    inp = make_inputs(w, seed=26, pad=3, ld_multiple=8)
+    D, _, _ = full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair")
+    if _pairs_resident() == 76:
+        assert lib.gemm_last_kernel() == "gemm_bf16_tc<pair,split-tail>"
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES[1:])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_cta_pair_split_tail_pieces_full(shape, dtype):
+    M, N, K = shape
+    w = Workload("pair_tail", M, N, K, 0.5, 1.0, dtype, ROW, COL, ROW)
+    inp = make_inputs(w, seed=27, ld_multiple=8)
+    full_check(w, inp, pad_d=4, expect_kernel=f"gemm_{dtype}_tc<pair")
+
+
+def test_cta_pair_split_tail_deterministic():
+    M, N, K = TAIL_SHAPES[2]
+    w = Workload("pair_tail_det", M, N, K, 0.5, 1.0, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=28)
+    D1, _, name = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert name.startswith("gemm_bf16_tc<pair")
+    assert torch.equal(D1, D2)
 
 
 # Split-K on the CUDA-core path: few tiles (every tile split along K) and a
