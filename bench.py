@@ -36,7 +36,9 @@ L2_BYTES = 129 * 1000 * 1000  # GB300 L2 (~129 MB)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "gemm_bf16_tc": "dense_gemm_08_gb300/csrc/gemm_tc.cu",
+    "gemm_f16_tc": "dense_gemm_08_gb300/csrc/gemm_tc.cu",
     "sgemm_simt": "dense_gemm_08_gb300/csrc/sgemm_simt.cu",
+    "skinny": "dense_gemm_08_gb300/csrc/skinny.cu",
 }
 
 
@@ -54,6 +56,18 @@ def roofline_tflops(flops, nbytes, peak_tflops, hbm_gbs):
     """min(peak, I * BW) in TFLOP/s, I = flops / bytes."""
     intensity = flops / nbytes
     return min(peak_tflops, intensity * hbm_gbs * 1e9 / 1e12)
+
+
+def hbm_bound_roof(roof, alg_bytes, seconds, hbm_gbs, peak_src, roof_tflops):
+    """The roofline object of a launch: when I x BW_HBM is below the compute
+    peak, the shape is HBM-bound and the fraction is taken against the HBM
+    bandwidth (algorithmic bytes / time); otherwise `roof` (compute) as is."""
+    if roof_tflops >= roof["peak"]:
+        return roof
+    achieved = alg_bytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "peak_source": f"{peak_src} HBM copy bandwidth",
+            "compute": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac")}}
 
 
 def fp32_core_peak_tflops(sms, mhz):
@@ -394,8 +408,10 @@ def bench_ours(args):
             roof["frac_at_run_clock"] = achieved / roof["peak_at_run_clock"]
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     alg = algorithmic_bytes(w.M, w.N, w.K, in_bytes, w.beta)
+    roof_tflops = roofline_tflops(w.flops, alg, peak, hbm)
+    roof = hbm_bound_roof(roof, alg, ms_per_step * 1e-3, hbm, peak_src, roof_tflops)
     roof["algorithmic_bytes"] = alg
-    roof["roof_min_peak_ibw"] = roofline_tflops(w.flops, alg, peak, hbm)
+    roof["roof_min_peak_ibw"] = roof_tflops
     roof["traffic"] = committed_traffic(kname, w.name)
     roof["kernel"] = kname
 

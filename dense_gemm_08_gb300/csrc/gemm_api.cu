@@ -125,9 +125,13 @@ GEMM_API gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, co
     const gemm::Problem p = normalise(M, N, K, alpha, A, lda, order_a, B, ldb, order_b, beta, C,
                                       ldc, D, ldd, order_cd);
     const char *name = "";
-    cudaError_t e = (K == 0 || alpha == 0.f)
-                        ? gemm::launch_scale_c(p, stream, &name)
-                        : gemm::launch_simt(p, gemm::InType::F32, stream, &name);
+    cudaError_t e;
+    if (K == 0 || alpha == 0.f)
+        e = gemm::launch_scale_c(p, stream, &name);
+    else if (gemm::skinny_eligible(p))
+        e = gemm::launch_skinny(p, gemm::InType::F32, stream, &name);
+    else
+        e = gemm::launch_simt(p, gemm::InType::F32, stream, &name);
     return finish(e, name);
 }
 
@@ -149,6 +153,8 @@ GEMM_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K, float a
         e = gemm::launch_scale_c(p, stream, &name);
     else if (gemm::tc_eligible(p))
         e = gemm::launch_tc(p, gemm::InType::BF16, stream, &name);
+    else if (gemm::skinny_eligible(p))
+        e = gemm::launch_skinny(p, gemm::InType::BF16, stream, &name);
     else
         e = gemm::launch_simt(p, gemm::InType::BF16, stream, &name);
     return finish(e, name);
@@ -172,6 +178,8 @@ GEMM_API gemm_status_t gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, float al
         e = gemm::launch_scale_c(p, stream, &name);
     else if (gemm::tc_eligible(p))
         e = gemm::launch_tc(p, gemm::InType::F16, stream, &name);
+    else if (gemm::skinny_eligible(p))
+        e = gemm::launch_skinny(p, gemm::InType::F16, stream, &name);
     else
         e = gemm::launch_simt(p, gemm::InType::F16, stream, &name);
     return finish(e, name);
@@ -210,6 +218,8 @@ GEMM_API gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K, floa
         e = gemm::launch_scale_c(p, stream, &name);
     else if (gemm::tc_eligible(p))
         e = gemm::launch_tc(p, gemm::InType::BF16, stream, &name);
+    else if (gemm::skinny_eligible(p))
+        e = gemm::launch_skinny(p, gemm::InType::BF16, stream, &name);
     else
         e = gemm::launch_simt(p, gemm::InType::BF16, stream, &name);
     return finish(e, name);

@@ -59,6 +59,12 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
 // Reads and clears the tensor-core kernel's device status word (after a sync).
 cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status);
 
+// GEMMs with at most kSkinnyMaxM rows (after the column-major D
+// normalisation): a kernel that streams op(B) once (skinny.cu).
+constexpr int64_t kSkinnyMaxM = 8;
+bool skinny_eligible(const Problem &p);
+cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, const char **name);
+
 // Peak probes (no memory traffic).  Each enqueues one kernel on `stream` and
 // stores the FLOPs it performs in *flops.
 //   launch_tc_probe: one CTA per SM (cta_group 1) or one CTA pair per two

@@ -38,6 +38,23 @@ def test_roofline_is_min_of_peak_and_intensity_times_bandwidth():
     assert bench.roofline_tflops(137438953472, q64, 20.0, 1000.0) == pytest.approx(15.875969, abs=1e-6)
 
 
+def test_hbm_bound_shapes_report_against_bandwidth():
+    compute = {"bound": "alu", "achieved": 0.3, "peak": 80.5, "unit": "TFLOP/s", "frac": 0.3 / 80.5}
+    # FP32 1 x 4096 x 4096, beta != 0: 67,158,016 B in 20 us -> 3357.9 GB/s
+    alg = bench.algorithmic_bytes(1, 4096, 4096, 4, -0.25)
+    flops = 2 * 4096 * 4096
+    roof_t = bench.roofline_tflops(flops, alg, 80.5, 6680.8)
+    r = bench.hbm_bound_roof(dict(compute), alg, 20e-6, 6680.8, "measured", roof_t)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(alg / 20e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6680.8)
+    assert r["compute"]["bound"] == "alu"
+    # a compute-bound shape keeps its compute roofline
+    big = bench.algorithmic_bytes(4096, 4096, 4096, 4, 0.0)
+    roof_t = bench.roofline_tflops(2 * 4096 ** 3, big, 80.5, 6680.8)
+    assert bench.hbm_bound_roof(dict(compute), big, 2.4e-3, 6680.8, "measured", roof_t) == compute
+
+
 def test_fp32_peak_formula():
     assert bench.fp32_core_peak_tflops(152, 2070.0) == pytest.approx(80.54784)
 

@@ -264,12 +264,14 @@ def test_small_integers_bit_exact(dtype, shape):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_tiny_shapes_brute_force(dtype):
-    """Every (M, N, K) in {1..5}^3, every storage order, two (alpha, beta)."""
-    for M, N, K in itertools.product(range(1, 6), repeat=3):
+    """Every (M, N, K) in {1..5, 9, 12} x {1..5}^2, every storage order, two
+    (alpha, beta): M <= 8 takes the small-M kernel, M = 9 and 12 the tiled
+    kernels (and a column-major D with N <= 5 the small-M kernel again)."""
+    for M, N, K in itertools.product([1, 2, 3, 4, 5, 9, 12], range(1, 6), range(1, 6)):
         for orders in ORDERS:
             for alpha, beta in ((1.0, 0.0), (1.5, -0.25)):
                 w = Workload("tiny", M, N, K, alpha, beta, dtype, *orders, dist="int")
-                # ld a multiple of 8 keeps BF16 on the tensor-core path
+                # ld a multiple of 8 keeps BF16 on the tensor-core path (M > 8)
                 inp = make_inputs(w, seed=M * 100 + N * 10 + K, ld_multiple=8)
                 Dbuf, _, name = run_gpu(w, inp)
                 ref, _ = oracle_full(w, inp)
