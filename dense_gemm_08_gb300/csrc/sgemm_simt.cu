@@ -64,6 +64,13 @@ struct SimtCfg {
 using BigCfg = SimtCfg<128, 256, 16, 2, 4, 4, 8, 4, 2, 1>;
 // 64 x 64 x 16 tile, 256 threads, 4 x 4 per thread: more CTAs for small problems.
 using SmallCfg = SimtCfg<64, 64, 16, 2, 4, 8, 4, 1, 1, 1>;
+// FP32 only: 128 x 128 x 16 tile, 8 x 8 per thread, for problems with too few
+// 128 x 256 tiles or a short K; and 256 x 64 x 16, 8 x 8 per thread, for a D
+// at most 64 columns wide.  Measured on GB300 against the two above: FP32
+// 127 x 8191 x 4096 29.4 -> 40.2 TFLOP/s (128 x 128), 4095 x 4097 x 1000
+// 38.6 -> 40.5 (128 x 128), 16384 x 64 x 8192 32.7 -> 46.5 (256 x 64).
+using WideCfg = SimtCfg<128, 128, 16, 2, 4, 8, 4, 2, 2, 1>;
+using TallCfg = SimtCfg<256, 64, 16, 4, 2, 8, 4, 2, 2, 1>;
 
 // ---- element access: FP32 values or BF16 bit patterns, widened to FP32 ----
 template <typename T>
@@ -642,13 +649,23 @@ __global__ void scale_c_kernel(const Problem p) {
 }  // namespace
 
 cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name) {
-    // Large tiles when they give at least one CTA per SM, small ones otherwise.
-    const int64_t big_tiles = ((p.M + BigCfg::BM - 1) / BigCfg::BM) *
-                              ((p.N + BigCfg::BN - 1) / BigCfg::BN);
-    const bool big = big_tiles >= sm_count();
-    if (in == InType::F32)
-        return big ? launch_cfg<BigCfg, float>(p, stream, name)
-                   : launch_cfg<SmallCfg, float>(p, stream, name);
+    auto tiles = [&p](int64_t bm, int64_t bn) {
+        return ((p.M + bm - 1) / bm) * ((p.N + bn - 1) / bn);
+    };
+    const int64_t sms = sm_count();
+    const bool big = tiles(BigCfg::BM, BigCfg::BN) >= sms;
+    if (in == InType::F32) {
+        // FP32: a D of at most 64 columns takes 256 x 64 tiles; 128 x 256
+        // tiles when there are two waves of them and K is long enough to
+        // carry their epilogue; else 128 x 128 tiles if there are enough of
+        // them for the stream-K tail to spread; else 64 x 64.
+        if (p.N <= TallCfg::BN) return launch_cfg<TallCfg, float>(p, stream, name);
+        if (tiles(BigCfg::BM, BigCfg::BN) >= 2 * sms && p.K >= 2048)
+            return launch_cfg<BigCfg, float>(p, stream, name);
+        if (tiles(WideCfg::BM, WideCfg::BN) * 4 >= sms)
+            return launch_cfg<WideCfg, float>(p, stream, name);
+        return launch_cfg<SmallCfg, float>(p, stream, name);
+    }
     if (in == InType::F16)
         return big ? launch_cfg<BigCfg, __half>(p, stream, name)
                    : launch_cfg<SmallCfg, __half>(p, stream, name);

@@ -392,6 +392,22 @@ def test_tma_store_edges_stay_inside_d(n):
         full_check(w, inp, pad_d=pad)
 
 
+# FP32 tile configurations: 128 x 256 (two waves, long K), 128 x 128 (few
+# big tiles or short K), 256 x 64 (D at most 64 wide), 64 x 64 (small);
+# ragged edges and stream-K tails in each.
+SIMT_CFG_SHAPES = [(2560, 5120, 2048), (1100, 1300, 700), (700, 900, 500), (1000, 64, 777),
+                   (3000, 33, 300), (130, 140, 150)]
+
+
+@pytest.mark.parametrize("shape", SIMT_CFG_SHAPES)
+def test_f32_tile_configurations_full(shape):
+    M, N, K = shape
+    for orders in (ORDERS if M * N * K < 2e9 else ORDERS[:2]):
+        w = Workload("f32cfg", M, N, K, 1.5, -0.25, "f32", *orders)
+        inp = make_inputs(w, seed=M + N + K, pad=1)
+        full_check(w, inp, pad_d=2, expect_kernel="sgemm_simt<f32")
+
+
 def test_f32_unaligned_leading_dimensions():
     """Leading dimensions that are not multiples of 4 (scalar loads and stores)."""
     for orders in [(ROW, ROW, ROW), (COL, COL, COL)]:
