@@ -197,6 +197,21 @@ __device__ __forceinline__ void stage_slice(float *__restrict__ xs, const float4
     }
 }
 
+// Two FP32 multiply-adds in one instruction (fma.rn.f32x2): each half is an
+// fmaf of its own, rounded the same way.  Pairs are 64-bit registers, low
+// half first.
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t dup2(float x) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 struct SimtArgs {
     Problem p;
     bool vec_a, vec_b;  // vector global loads of A / B are aligned
@@ -282,11 +297,13 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
         const int64_t m0 = tm * BM, n0 = tn * BN;
         const bool edge_mn = (m0 + BM > p.M) || (n0 + BN > p.N);
 
-        float acc[TM][TN];
+        // accumulators as row pairs (2p, 2p + 1) for the paired FMAs; unpacked
+        // into acc[TM][TN] after the K loop
+        uint64_t acc2[TM / 2][TN];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+            for (int j = 0; j < TN; ++j) acc2[i][j] = 0ull;
 
         SliceLoader<T, AK, BM, BK, NT, Cfg::SLOTS_A> la;
         SliceLoader<T, BKM, BN, BK, NT, Cfg::SLOTS_B> lb;
@@ -319,17 +336,18 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             const float *as = As[cur];
             const float *bs = Bs[cur];
             // fragments double-buffered in registers: slice row k + 1 is read
-            // from shared memory while row k is multiplied
-            float a[2][TM], b[2][TN];
+            // from shared memory while row k is multiplied.  A's fragment is
+            // read as row pairs (a quad of rows = two pairs), B's values are
+            // duplicated into pairs: one paired FMA updates rows 2p, 2p + 1.
+            uint64_t a[2][TM / 2];
+            float b[2][TN];
             auto load_frag = [&](int buf, int k) {
 #pragma unroll
                 for (int q = 0; q < Cfg::QM; ++q) {
-                    const float4 v =
-                        *reinterpret_cast<const float4 *>(&as[k * SA + a_off + q * Cfg::LM * 4]);
-                    a[buf][q * 4 + 0] = v.x;
-                    a[buf][q * 4 + 1] = v.y;
-                    a[buf][q * 4 + 2] = v.z;
-                    a[buf][q * 4 + 3] = v.w;
+                    const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(
+                        &as[k * SA + a_off + q * Cfg::LM * 4]);
+                    a[buf][q * 2 + 0] = v.x;
+                    a[buf][q * 2 + 1] = v.y;
                 }
 #pragma unroll
                 for (int q = 0; q < Cfg::QN; ++q) {
@@ -346,10 +364,11 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             for (int k = 0; k < BK; ++k) {
                 if (k + 1 < BK) load_frag((k + 1) & 1, k + 1);
 #pragma unroll
-                for (int i = 0; i < TM; ++i)
+                for (int j = 0; j < TN; ++j) {
+                    const uint64_t bj = dup2(b[k & 1][j]);
 #pragma unroll
-                    for (int j = 0; j < TN; ++j)
-                        acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
+                    for (int i = 0; i < TM / 2; ++i) fma2(acc2[i][j], a[k & 1][i], bj);
+                }
             }
             if (more) {
                 stage_slice<AK, BM, BK, NT, Cfg::SLOTS_A, SA>(As[cur ^ 1], ra);
@@ -358,6 +377,11 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             __syncthreads();
         }
         }
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) unpack2(acc2[i][j], acc[2 * i][j], acc[2 * i + 1][j]);
 
         if (split >= 0) {
             // Every contributor of a split tile stores its partial sums (each
