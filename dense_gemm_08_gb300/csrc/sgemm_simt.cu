@@ -338,9 +338,10 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             // fragments double-buffered in registers: slice row k + 1 is read
             // from shared memory while row k is multiplied.  A's fragment is
             // read as row pairs (a quad of rows = two pairs), B's values are
-            // duplicated into pairs: one paired FMA updates rows 2p, 2p + 1.
+            // duplicated into pairs as they are read (a step ahead of their
+            // use): one paired FMA updates rows 2p, 2p + 1.
             uint64_t a[2][TM / 2];
-            float b[2][TN];
+            uint64_t bd[2][TN];
             auto load_frag = [&](int buf, int k) {
 #pragma unroll
                 for (int q = 0; q < Cfg::QM; ++q) {
@@ -353,10 +354,10 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
                 for (int q = 0; q < Cfg::QN; ++q) {
                     const float4 v =
                         *reinterpret_cast<const float4 *>(&bs[k * SB + b_off + q * Cfg::LN * 4]);
-                    b[buf][q * 4 + 0] = v.x;
-                    b[buf][q * 4 + 1] = v.y;
-                    b[buf][q * 4 + 2] = v.z;
-                    b[buf][q * 4 + 3] = v.w;
+                    bd[buf][q * 4 + 0] = dup2(v.x);
+                    bd[buf][q * 4 + 1] = dup2(v.y);
+                    bd[buf][q * 4 + 2] = dup2(v.z);
+                    bd[buf][q * 4 + 3] = dup2(v.w);
                 }
             };
             load_frag(0, 0);
@@ -364,11 +365,9 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
             for (int k = 0; k < BK; ++k) {
                 if (k + 1 < BK) load_frag((k + 1) & 1, k + 1);
 #pragma unroll
-                for (int j = 0; j < TN; ++j) {
-                    const uint64_t bj = dup2(b[k & 1][j]);
+                for (int j = 0; j < TN; ++j)
 #pragma unroll
-                    for (int i = 0; i < TM / 2; ++i) fma2(acc2[i][j], a[k & 1][i], bj);
-                }
+                    for (int i = 0; i < TM / 2; ++i) fma2(acc2[i][j], a[k & 1][i], bd[k & 1][j]);
             }
             if (more) {
                 stage_slice<AK, BM, BK, NT, Cfg::SLOTS_A, SA>(As[cur ^ 1], ra);
