@@ -9,7 +9,7 @@ first call (there is no CPU fallback).
 Same names as the C ABI:
     gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_bf16_f32acc_ex,
     gemm_f32_noalloc, gemm_status_string, gemm_last_device_status, gemm_last_kernel,
-    gemm_probe_tc_bf16, gemm_probe_fma_f32
+    gemm_probe_tc_bf16, gemm_probe_fma_f32, gemm_probe_wait_timeout
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
 (torch's current stream).  A non-zero status raises ``GemmError``.
@@ -36,7 +36,8 @@ GEMM_ERR_INTERNAL = 5
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
 EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_bf16_f32acc_ex",
             "gemm_f32_noalloc", "gemm_status_string", "gemm_last_device_status",
-            "gemm_last_kernel", "gemm_probe_tc_bf16", "gemm_probe_fma_f32")
+            "gemm_last_kernel", "gemm_probe_tc_bf16", "gemm_probe_fma_f32",
+            "gemm_probe_wait_timeout")
 
 GEMM_ACT_NONE = 0
 GEMM_ACT_RELU = 1
@@ -92,6 +93,8 @@ def library() -> ctypes.CDLL:
             lib.gemm_probe_tc_bf16.restype = ip
             lib.gemm_probe_fma_f32.argtypes = [i64, dp, vp]
             lib.gemm_probe_fma_f32.restype = ip
+            lib.gemm_probe_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+            lib.gemm_probe_wait_timeout.restype = ip
             _lib = lib
     return _lib
 
@@ -197,6 +200,14 @@ def gemm_probe_fma_f32(trips, stream=None, check=True):
     if check and st != GEMM_OK:
         raise GemmError(st, "gemm_probe_fma_f32")
     return st, flops.value
+
+
+def gemm_probe_wait_timeout(timeout_ns, stream=None, check=True):
+    """Enqueue the bounded-wait probe (a wait that runs out after timeout_ns)."""
+    st = library().gemm_probe_wait_timeout(int(timeout_ns), _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_probe_wait_timeout")
+    return st
 
 
 # ------------------------------------------------------------ torch helper

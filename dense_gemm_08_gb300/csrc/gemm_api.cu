@@ -283,6 +283,14 @@ GEMM_API gemm_status_t gemm_probe_tc_bf16(int cta_group, int64_t n_mma, double *
                   cta_group == 2 ? "tc_probe<pair>" : "tc_probe");
 }
 
+GEMM_API gemm_status_t gemm_probe_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+    t_last_kernel = "";
+    if (timeout_ns < 1000 || timeout_ns > 10ull * 1000 * 1000 * 1000) return GEMM_ERR_INVALID_VALUE;
+    const gemm_status_t dev = check_device();
+    if (dev != GEMM_OK) return dev;
+    return finish(gemm::launch_wait_probe(timeout_ns, stream), "wait_probe");
+}
+
 GEMM_API gemm_status_t gemm_probe_fma_f32(int64_t trips, double *flops, cudaStream_t stream) {
     t_last_kernel = "";
     if (trips < 1 || trips > (int64_t(1) << 40) || flops == nullptr) return GEMM_ERR_INVALID_VALUE;

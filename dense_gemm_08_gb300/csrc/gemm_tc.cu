@@ -1051,6 +1051,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) tmem_dealloc<CG>(tmem_base);
 }
 
+// ------------------------------------------------------- bounded-wait probe
+// One thread waits, with the kernels' bounded wait, on an mbarrier that
+// nothing arrives on; after timeout_ns it gives up and sets the device status
+// word exactly as a GEMM whose wait ran out would.  Nothing else is in flight.
+__global__ void wait_probe_kernel(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_addr(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const volatile int never = 0;
+    if (!wait_bounded(smem_addr(&bar), 0, &never, timeout_ns)) atomicExch(&g_tc_status, 1);
+}
+
 // -------------------------------------------------------- tensor-pipe probe
 // The tensor pipe with no memory traffic: each CTA (pair) writes one A tile
 // (128 x 64) and one B tile (B_ROWS x 64) of BF16 values into shared memory
@@ -1465,6 +1478,11 @@ cudaError_t launch_tc_probe(int cta_group, int64_t n_mma, cudaStream_t stream, d
     }
     if (e != cudaSuccess) return e;
     *flops = mma_flops * static_cast<double>(n_mma) * groups;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(uint64_t timeout_ns, cudaStream_t stream) {
+    wait_probe_kernel<<<1, 32, 0, stream>>>(timeout_ns);
     return cudaGetLastError();
 }
 

@@ -73,5 +73,8 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
 //     16 x trips dependent FP32 FMAs.
 cudaError_t launch_tc_probe(int cta_group, int64_t n_mma, cudaStream_t stream, double *flops);
 cudaError_t launch_fma_probe(int64_t trips, cudaStream_t stream, double *flops);
+// One CTA waiting on an mbarrier that nothing completes: its bounded wait
+// gives up after timeout_ns and sets the tensor-core status word.
+cudaError_t launch_wait_probe(uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace gemm

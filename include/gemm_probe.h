@@ -23,6 +23,9 @@
  * device.  The caller times the launch (for example with CUDA events on
  * `stream`) and divides.  The values the kernels compute are discarded.
  *
+ * A third probe, gemm_probe_wait_timeout, exercises the kernels' failure
+ * path (a bounded wait that runs out) without breaking a kernel.
+ *
  * Errors (returned before any launch unless noted):
  *   GEMM_ERR_INVALID_VALUE       a count outside [1, 2^40], cta_group not 1
  *                                or 2, or flops == NULL
@@ -58,6 +61,18 @@ gemm_status_t gemm_probe_tc_bf16(int cta_group, int64_t n_mma, double *flops,
  * 16 x trips dependent FP32 FMAs.  *flops = 2 x 8 x 16 x trips x threads.
  */
 gemm_status_t gemm_probe_fma_f32(int64_t trips, double *flops, cudaStream_t stream);
+
+/*
+ * The kernels' failure path, exercised without breaking a kernel: one thread
+ * waits, with the same bounded wait the GEMM kernels use, on a barrier that
+ * nothing completes; after timeout_ns (1 us .. 10 s) it gives up and sets the
+ * device status word, so that gemm_last_device_status returns
+ * GEMM_ERR_TIMEOUT (and clears the word).  Nothing else is in flight and the
+ * CUDA context stays usable.  Enqueues one kernel on `stream`.
+ * Errors: GEMM_ERR_INVALID_VALUE (timeout out of range),
+ * GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_LAUNCH.
+ */
+gemm_status_t gemm_probe_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,8 @@ def test_probe_argument_errors_without_a_device():
     for trips in [0, -1, 1 << 41]:
         st, _ = lib.gemm_probe_fma_f32(trips, stream=0, check=False)
         assert st == lib.GEMM_ERR_INVALID_VALUE, trips
+    for t in [0, 999, 11 * 10 ** 9]:
+        assert lib.gemm_probe_wait_timeout(t, stream=0, check=False) == lib.GEMM_ERR_INVALID_VALUE
     # a NULL flops pointer is refused
     assert lib.library().gemm_probe_fma_f32(10, None, None) == lib.GEMM_ERR_INVALID_VALUE
     assert lib.library().gemm_probe_tc_bf16(1, 10, None, None) == lib.GEMM_ERR_INVALID_VALUE

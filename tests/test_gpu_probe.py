@@ -65,3 +65,18 @@ def test_probe_leaves_gemm_results_intact():
     d = lib.gemm(a.cuda(), b.t().contiguous().cuda().t())
     ref = a.double() @ b.double()
     assert torch.equal(d.cpu().double(), ref)
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """The failure path without a broken kernel: a wait on a barrier nothing
+    completes gives up after 5 ms, the status word says GEMM_ERR_TIMEOUT once,
+    and the context stays usable (a GEMM afterwards is exact)."""
+    import time
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    t0 = time.perf_counter()
+    assert lib.gemm_probe_wait_timeout(5_000_000) == lib.GEMM_OK
+    assert lib.gemm_last_kernel() == "wait_probe"
+    assert lib.gemm_last_device_status() == lib.GEMM_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert lib.gemm_last_device_status() == lib.GEMM_OK  # read and cleared
+    test_probe_leaves_gemm_results_intact()
