@@ -265,7 +265,12 @@ GEMM_API const char *gemm_status_string(gemm_status_t status) {
 GEMM_API gemm_status_t gemm_last_device_status(cudaStream_t stream) {
     int status = 0;
     if (gemm::tc_read_and_clear_status(stream, &status) != cudaSuccess) return GEMM_ERR_INTERNAL;
-    return status ? GEMM_ERR_TIMEOUT : GEMM_OK;
+    if (status) {
+        // a kernel that gave up may have left split counters mid-count
+        if (gemm::split_sync_reset_device() != cudaSuccess) return GEMM_ERR_INTERNAL;
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
 }
 
 GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }

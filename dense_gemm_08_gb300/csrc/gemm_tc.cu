@@ -97,7 +97,9 @@ struct TcArgs {
     int64_t tail_first;
     int tail_ks;
     float *ws;
-    int *ws_count;
+    int *ws_count;      // the stream's split counters: zero between calls
+    unsigned *ws_flag;  // CG = 1 split-K: [tile * 4 + warp] = generation once all pieces are in
+    unsigned generation;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -828,6 +830,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int *const counter =
                     args.ws_count + (CG == 1 ? t * 4 + quarter
                                              : ((t - args.tail_first) * 2 + rank) * 4 + quarter);
+                unsigned *const flag = args.ws_flag + t * 4 + quarter;  // CG = 1 only
 #pragma unroll 1
                 for (int chunk = 0; chunk < n_chunks; ++chunk) {
                     uint8_t *box = boxes + (nb & 1) * 4096;
@@ -851,14 +854,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     bulk_wait_all();  // the partial sums are in global memory
                     __threadfence();
                     const int before = atomicAdd(counter, 1);
+                    const bool last_in = before == it.nsp - 1;
+                    if (last_in) *counter = 0;  // all pieces counted: ready for the next call
                     if (CG == 1) {
                         // 2) wait until all ks pieces are published (all
-                        // resident: one CTA per SM, cooperative launch)
+                        // resident: one CTA per SM, cooperative launch); the
+                        // last one to be counted raises the tile's flag to
+                        // this call's generation
+                        if (last_in) {
+                            __threadfence();
+                            atomicExch(flag, args.generation);
+                        }
                         reduce = sp < n_chunks;
-                        if (reduce) {
-                            const volatile int *cnt = counter;
+                        if (reduce && !last_in) {
+                            const volatile unsigned *fl = flag;
                             const uint64_t t0 = global_timer();
-                            while (*cnt < it.nsp) {
+                            while (*fl != args.generation) {
                                 if (*abort_flag || global_timer() - t0 > args.timeout_ns) {
                                     ok2 = 0;
                                     break;
@@ -867,7 +878,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     } else {
-                        reduce = before == it.nsp - 1;  // the last piece reduces
+                        reduce = last_in;  // the last piece reduces
                     }
                     if (reduce) __threadfence();
                 }
@@ -1343,6 +1354,8 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.tail_ks = 1;
     a.ws = nullptr;
     a.ws_count = nullptr;
+    a.ws_flag = nullptr;
+    a.generation = 0;
     a.ab_format = bf16 ? 1 : 0;
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
@@ -1367,18 +1380,15 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         void *ws = nullptr;
         if (tail_ks > 1) {
             *name = bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>";
+            // counters: per tail tile 2 CTAs x 4 warps (the stream's, zero)
+            e = split_sync(stream, static_cast<size_t>(tail) * 2 * 4, 0, &a.ws_count, nullptr,
+                           nullptr);
+            if (e != cudaSuccess) return e;
             // per tail tile and piece: 2 CTAs x 4 warps x 8 boxes of 4 KiB
             const size_t part_bytes = static_cast<size_t>(tail) * tail_ks * 2 * 4 * 8 * 4096;
-            const size_t count_bytes = static_cast<size_t>(tail) * 2 * 4 * sizeof(int);
-            e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            e = workspace_alloc(part_bytes, stream, &ws);
             if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
-            a.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
-            e = cudaMemsetAsync(a.ws_count, 0, count_bytes, stream);
-            if (e != cudaSuccess) {
-                workspace_free(ws, stream);
-                return e;
-            }
         }
         e = launch_variant<2>(p, a, 2 * d->pairs, stream);
         if (ws != nullptr) {
@@ -1401,17 +1411,15 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         }
         void *ws = nullptr;
         if (ks > 1) {
+            // counters and flags: per tile 4 warps (the stream's: counters
+            // zero, flags below this call's generation)
+            e = split_sync(stream, static_cast<size_t>(tiles) * 4, static_cast<size_t>(tiles) * 4,
+                           &a.ws_count, &a.ws_flag, &a.generation);
+            if (e != cudaSuccess) return e;
             const size_t part_bytes = static_cast<size_t>(tiles) * ks * 4 * 8 * 4096;
-            const size_t count_bytes = static_cast<size_t>(tiles) * 4 * sizeof(int);
-            e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            e = workspace_alloc(part_bytes, stream, &ws);
             if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
-            a.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
-            e = cudaMemsetAsync(a.ws_count, 0, count_bytes, stream);
-            if (e != cudaSuccess) {
-                workspace_free(ws, stream);
-                return e;
-            }
             a.ks = static_cast<int>(ks);
             *name = bf16 ? "gemm_bf16_tc<splitk>" : "gemm_f16_tc<splitk>";
         } else {

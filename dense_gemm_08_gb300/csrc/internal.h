@@ -38,6 +38,16 @@ enum class InType { F32, BF16, F16 };
 // and returned on `stream` once the kernels enqueued before the free are done.
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr);
 cudaError_t workspace_free(void *ptr, cudaStream_t stream);
+// The split kernels' counters and flags for `stream` on the current device:
+// at least n_counters ints that are zero (every kernel returns the counters it
+// uses to zero) and n_flags unsigned flags, with the generation number of this
+// call (a flag equal to it was set by this call).  Calls on one stream are
+// ordered, so they may share the buffers; calls on different streams do not.
+cudaError_t split_sync(cudaStream_t stream, size_t n_counters, size_t n_flags, int **counters,
+                       unsigned **flags, unsigned *generation);
+// After a bounded wait ran out (counters may be left mid-count): zero every
+// stream's counters and flags of the current device (synchronises the device).
+cudaError_t split_sync_reset_device();
 
 // Each launcher enqueues one kernel on `stream`, returns the CUDA error of
 // the launch and sets *name to the kernel's static name.

@@ -609,15 +609,14 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
             const cudaError_t e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
             if (e != cudaSuccess) return e;
         } else {
-            cudaError_t e = workspace_alloc(part_bytes + count_bytes, stream, &ws);
+            // partial sums from the pool; counters from the stream's split
+            // counters (zero; the last contributor of a tile resets its own)
+            cudaError_t e = split_sync(stream, static_cast<size_t>(plan.tail_tiles), 0,
+                                       &args.ws_count, nullptr, nullptr);
+            if (e != cudaSuccess) return e;
+            e = workspace_alloc(part_bytes, stream, &ws);
             if (e != cudaSuccess) return e;
             args.ws_part = static_cast<float *>(ws);
-            args.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes);
-            e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
-            if (e != cudaSuccess) {
-                workspace_free(ws, stream);
-                return e;
-            }
         }
     }
 

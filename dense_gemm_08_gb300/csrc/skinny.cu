@@ -121,7 +121,7 @@ struct SkinnyArgs {
     int n_slices;
     bool vec_b;     // B's rows (N-contiguous) or columns (K-contiguous) allow wide loads
     float *ws;      // [n_slices][M][N] partial sums (n_slices > 1)
-    int *ws_count;  // [n_cb] slices counted per column block
+    int *ws_count;  // [n_cb] slices counted per column block (zero between calls)
 };
 
 __device__ __forceinline__ float a_elem(const Problem &p, int m, int64_t k, int in_type) {
@@ -195,6 +195,7 @@ __device__ __forceinline__ void finish_unit(const SkinnyArgs &a, const float *ou
     if (threadIdx.x == 0) s_last = atomicAdd(&a.ws_count[cb], 1) == a.n_slices - 1;
     __syncthreads();
     if (!s_last) return;
+    if (threadIdx.x == 0) a.ws_count[cb] = 0;  // every slice counted: ready for the next call
     __threadfence();
     for (int idx = threadIdx.x; idx < total; idx += kThreads) {
         const int m = idx / NB, jj = idx % NB;
@@ -441,18 +442,15 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
 
     void *ws = nullptr;
     if (a.n_slices > 1) {
-        const size_t part = (static_cast<size_t>(a.n_slices) * p.M * p.N * sizeof(float) + 255) &
-                            ~static_cast<size_t>(255);
-        const size_t count = static_cast<size_t>(a.n_cb) * sizeof(int);
-        cudaError_t e = workspace_alloc(part + count, stream, &ws);
+        // partial sums from the pool; counters from the stream's split
+        // counters (zero; the last slice of a column block resets its own)
+        cudaError_t e = split_sync(stream, static_cast<size_t>(a.n_cb), 0, &a.ws_count, nullptr,
+                                   nullptr);
+        if (e != cudaSuccess) return e;
+        const size_t part = static_cast<size_t>(a.n_slices) * p.M * p.N * sizeof(float);
+        e = workspace_alloc(part, stream, &ws);
         if (e != cudaSuccess) return e;
         a.ws = static_cast<float *>(ws);
-        a.ws_count = reinterpret_cast<int *>(static_cast<char *>(ws) + part);
-        e = cudaMemsetAsync(a.ws_count, 0, count, stream);
-        if (e != cudaSuccess) {
-            workspace_free(ws, stream);
-            return e;
-        }
     }
     const unsigned g = static_cast<unsigned>(grid);
     if (in == InType::F32) {

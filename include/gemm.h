@@ -236,7 +236,10 @@ const char *gemm_status_string(gemm_status_t status);
  * the current device's status word.  Returns GEMM_OK, or GEMM_ERR_TIMEOUT if
  * a tensor-core launch on this device gave up a bounded wait since the last
  * read (its D is then incomplete), or GEMM_ERR_INTERNAL if the read itself
- * failed.
+ * failed.  After a timeout it also returns the device's split counters (the
+ * counts of finished K pieces that each stream keeps between calls, and that
+ * a kernel which gave up may have left mid-count) to zero, synchronising the
+ * device; read it after a timeout before the next call on this device.
  */
 gemm_status_t gemm_last_device_status(cudaStream_t stream);
 

@@ -1,0 +1,115 @@
+"""GPU tests of the split kernels' per-stream counters.
+
+Every kernel that splits a tile's K range (tensor-core split-K, the CTA-pair
+kernel's split last round, the CUDA-core stream-K tail, the small-M kernel's
+K slices) counts the finished pieces in counters that belong to the stream
+and persist between calls; the piece that completes a count returns it to
+zero, so no call clears them.  These tests check that calls of every variant,
+back to back in any order, on two streams at once, and after a kernel gave up
+a bounded wait, give the same bits as a first call that is checked against
+the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_08_gb300 as lib
+from dense_gemm_08_gb300.inputs import COL, ROW, Workload, make_inputs, output_buffer
+from gemm_harness import assert_within, oracle_points, sample_points
+
+pytestmark = pytest.mark.gpu
+
+# (workload, expected kernel prefix)
+CASES = [
+    (Workload("tc_splitk", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW), "gemm_bf16_tc<splitk>"),
+    (Workload("pair_tail", 2048, 3072, 768, 0.5, 1.0, "bf16", ROW, COL, ROW), "gemm_bf16_tc<pair"),
+    (Workload("f16_splitk", 300, 600, 2048, 1.0, 0.5, "f16", COL, ROW, COL), "gemm_f16_tc<splitk>"),
+    (Workload("simt_splitk", 384, 384, 1000, 1.5, -0.25, "f32", ROW, ROW, ROW), "sgemm_simt<f32"),
+    (Workload("simt_tail", 2560, 2048, 512, 1.0, 0.0, "f32", ROW, COL, ROW), "sgemm_simt<f32"),
+    (Workload("skinny", 4, 3000, 5000, 1.5, -0.25, "f32", ROW, ROW, ROW), "skinny<f32"),
+]
+
+FN = {"f32": lib.gemm_f32, "bf16": lib.gemm_bf16_f32acc, "f16": lib.gemm_f16_f32acc}
+
+
+class Case:
+    """Device copies of one workload's inputs, and a launcher into fresh D buffers."""
+
+    def __init__(self, w, prefix, seed):
+        self.w, self.prefix = w, prefix
+        self.inp = make_inputs(w, seed=seed, ld_multiple=8)
+        self.A = self.inp["A"].cuda()
+        self.B = self.inp["B"].cuda()
+        self.C = self.inp["C"].cuda() if self.inp["C"] is not None else None
+
+    def launch(self, stream=None):
+        D, ldd = output_buffer(self.w, device="cuda", fill=0.0)
+        w, inp = self.w, self.inp
+        FN[w.dtype](w.M, w.N, w.K, w.alpha, self.A, inp["lda"], w.order_a, self.B, inp["ldb"],
+                    w.order_b, w.beta, self.C, inp["ldc"], D, ldd, w.order_cd, stream)
+        assert lib.gemm_last_kernel().startswith(self.prefix), lib.gemm_last_kernel()
+        return D
+
+    def check_against_oracle(self, D):
+        w = self.w
+        Dl = D.cpu().numpy() if w.order_cd == ROW else D.cpu().numpy().T
+        I, J = sample_points(w.M, w.N, np.random.default_rng(5), n_random=1500)
+        ref, S = oracle_points(w, self.inp, I, J)
+        C = self.inp["C_logical"].numpy()[I, J] if self.inp["C_logical"] is not None else None
+        assert_within(w, Dl[I, J], ref, S, C, "first call")
+
+
+@pytest.fixture(scope="module")
+def cases():
+    out = [Case(w, prefix, seed=40 + i) for i, (w, prefix) in enumerate(CASES)]
+    torch.cuda.synchronize()
+    return out
+
+
+def _first_results(cases):
+    first = [c.launch() for c in cases]
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    return first
+
+
+def test_back_to_back_calls_of_every_split_variant(cases):
+    first = _first_results(cases)
+    for c, D in zip(cases, first):
+        c.check_against_oracle(D)
+    order = np.random.default_rng(3).permutation(np.repeat(np.arange(len(cases)), 4))
+    got = [(i, cases[i].launch()) for i in order]  # no synchronisation in between
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    for i, D in got:
+        assert torch.equal(D, first[i]), cases[i].w.name
+
+
+def test_two_streams_at_once(cases):
+    first = _first_results(cases)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream())
+    got = []
+    for rep in range(3):
+        for i in range(len(cases)):
+            j = (i + 1 + rep) % len(cases)
+            with torch.cuda.stream(s1):
+                got.append((i, cases[i].launch(s1)))
+            with torch.cuda.stream(s2):
+                got.append((j, cases[j].launch(s2)))
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    for i, D in got:
+        assert torch.equal(D, first[i]), cases[i].w.name
+
+
+def test_split_variants_after_a_wait_gave_up(cases):
+    first = _first_results(cases)
+    assert lib.gemm_probe_wait_timeout(2_000_000) == lib.GEMM_OK
+    # reading the timeout also returns every split counter on the device to zero
+    assert lib.gemm_last_device_status() == lib.GEMM_ERR_TIMEOUT
+    got = [(i, c.launch()) for i, c in enumerate(cases)]
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    for i, D in got:
+        assert torch.equal(D, first[i]), cases[i].w.name
