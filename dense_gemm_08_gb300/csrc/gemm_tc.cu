@@ -651,6 +651,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t li = 0;
             bool ok = true;
+            // The tensor pipe idles while this thread runs anything between
+            // two stages' MMAs, so the loop keeps that short: barrier
+            // addresses and stage-0 descriptors are fixed here (stage s adds
+            // s x the stage size, K slice kk adds kk x the step, in 16-byte
+            // units), and it waits for two stages at a time, then issues
+            // their 8 MMAs back to back.
+            const uint32_t full0 = smem_addr(&full[0]), empty0 = smem_addr(&empty[0]);
+            const uint64_t a_desc0 = args.a_kmajor ? desc_kmajor(ring_base, 0) : desc_mnmajor(ring_base, 0);
+            const uint64_t b_desc0 = args.b_kmajor ? desc_kmajor(ring_base + C::A_BYTES, 0)
+                                                   : desc_mnmajor(ring_base + C::A_BYTES, 0);
+            const uint64_t a_step = args.a_kmajor ? (UMMA_K * 2) >> 4 : (UMMA_K * 128) >> 4;
+            const uint64_t b_step = args.b_kmajor ? (UMMA_K * 2) >> 4 : (UMMA_K * 128) >> 4;
             for (int64_t w = group_id; w < n_items && ok; w += num_groups, ++li) {
                 const WorkItem it = work_item<CG>(w, args);
                 const int64_t kb_begin = it.kb_begin;
@@ -665,26 +677,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bounded(smem_addr(&full[stage]), phase, abort_flag,
-                                      args.timeout_ns)) {
+                static_assert(BK / UMMA_K == 4, "four MMAs per stage below");
+                const int nkb = static_cast<int>(kb_end - kb_begin);
+                for (int i = 0; i < nkb; i += 2) {
+                    const bool two = i + 1 < nkb;
+                    const int s0 = stage;
+                    const uint32_t p0 = phase;
+                    const int s1 = s0 + 1 == C::STAGES ? 0 : s0 + 1;
+                    const uint32_t p1 = s1 == 0 ? p0 ^ 1u : p0;
+                    const uint32_t fb0 = full0 + 8u * static_cast<uint32_t>(s0);
+                    const uint32_t fb1 = full0 + 8u * static_cast<uint32_t>(s1);
+                    if (!mbar_try_wait(fb0, p0) && !wait_bounded(fb0, p0, abort_flag, args.timeout_ns)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    if (two && !mbar_try_wait(fb1, p1) &&
+                        !wait_bounded(fb1, p1, abort_flag, args.timeout_ns)) {
                         raise_abort(abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = ring_base + stage * C::STAGE_BYTES;
-                    const uint32_t sb = sa + C::A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = args.a_kmajor ? desc_kmajor(sa, kk) : desc_mnmajor(sa, kk);
-                        const uint64_t bd = args.b_kmajor ? desc_kmajor(sb, kk) : desc_mnmajor(sb, kk);
-                        tc_mma<CG>(d_tmem, ad, bd, idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+                    uint64_t ad = a_desc0 + static_cast<uint64_t>(s0) * (C::STAGE_BYTES >> 4);
+                    uint64_t bd = b_desc0 + static_cast<uint64_t>(s0) * (C::STAGE_BYTES >> 4);
+                    tc_mma<CG>(d_tmem, ad, bd, idesc, i > 0 ? 1u : 0u);
+                    tc_mma<CG>(d_tmem, ad + a_step, bd + b_step, idesc, 1u);
+                    tc_mma<CG>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, idesc, 1u);
+                    tc_mma<CG>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, idesc, 1u);
+                    if (two) {
+                        ad = a_desc0 + static_cast<uint64_t>(s1) * (C::STAGE_BYTES >> 4);
+                        bd = b_desc0 + static_cast<uint64_t>(s1) * (C::STAGE_BYTES >> 4);
+                        tc_mma<CG>(d_tmem, ad, bd, idesc, 1u);
+                        tc_mma<CG>(d_tmem, ad + a_step, bd + b_step, idesc, 1u);
+                        tc_mma<CG>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, idesc, 1u);
+                        tc_mma<CG>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, idesc, 1u);
                     }
-                    tc_commit<CG>(smem_addr(&empty[stage]));  // frees the stage (in both CTAs)
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1;
+                    tc_commit<CG>(empty0 + 8u * static_cast<uint32_t>(s0));  // frees the stages (both CTAs)
+                    if (two) tc_commit<CG>(empty0 + 8u * static_cast<uint32_t>(s1));
+                    if (two) {
+                        stage = s1 + 1 == C::STAGES ? 0 : s1 + 1;
+                        phase = stage == 0 ? p1 ^ 1u : p1;
+                    } else {
+                        stage = s1;
+                        phase = p1;
                     }
                 }
                 if (!ok) break;
