@@ -38,13 +38,19 @@ enum class InType { F32, BF16, F16 };
 // and returned on `stream` once the kernels enqueued before the free are done.
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr);
 cudaError_t workspace_free(void *ptr, cudaStream_t stream);
-// The split kernels' counters and flags for `stream` on the current device:
-// at least n_counters ints that are zero (every kernel returns the counters it
-// uses to zero) and n_flags unsigned flags, with the generation number of this
-// call (a flag equal to it was set by this call).  Calls on one stream are
-// ordered, so they may share the buffers; calls on different streams do not.
+// The split kernels' counters and flags for one launch on `stream` (current
+// device): at least n_counters ints that are zero and n_flags unsigned flags
+// that are below *generation, the number this launch writes to a flag.
+//   Eager calls get the stream's persistent buffers and enqueue nothing:
+//   every kernel returns the counters it used to zero, and calls on one
+//   stream run in order, so they may share them (calls on other streams
+//   have their own).  *owned = nullptr.
+//   Under stream capture a graph may be replayed on any stream, at the same
+//   time as other work, with the generation fixed at capture: the call gets a
+//   fresh zeroed block from the pool instead (*owned = its address, generation
+//   1), which the caller frees in stream order after its launch.
 cudaError_t split_sync(cudaStream_t stream, size_t n_counters, size_t n_flags, int **counters,
-                       unsigned **flags, unsigned *generation);
+                       unsigned **flags, unsigned *generation, void **owned);
 // After a bounded wait ran out (counters may be left mid-count): zero every
 // stream's counters and flags of the current device (synchronises the device).
 cudaError_t split_sync_reset_device();

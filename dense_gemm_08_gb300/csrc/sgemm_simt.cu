@@ -597,6 +597,7 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
 
     // workspace for the dealt-out tiles: partial sums, then one counter per tile
     void *ws = nullptr;
+    void *sync_owned = nullptr;  // counters of a captured launch (see split_sync)
     if (plan.tail_tiles > 0) {
         const size_t part_bytes = align256(static_cast<size_t>(plan.tail_tiles) *
                                            plan.max_contrib * Cfg::BM * Cfg::BN * sizeof(float));
@@ -612,10 +613,13 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
             // partial sums from the pool; counters from the stream's split
             // counters (zero; the last contributor of a tile resets its own)
             cudaError_t e = split_sync(stream, static_cast<size_t>(plan.tail_tiles), 0,
-                                       &args.ws_count, nullptr, nullptr);
+                                       &args.ws_count, nullptr, nullptr, &sync_owned);
             if (e != cudaSuccess) return e;
             e = workspace_alloc(part_bytes, stream, &ws);
-            if (e != cudaSuccess) return e;
+            if (e != cudaSuccess) {
+                if (sync_owned != nullptr) workspace_free(sync_owned, stream);
+                return e;
+            }
             args.ws_part = static_cast<float *>(ws);
         }
     }
@@ -645,8 +649,9 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
         *name = names[kind][3];
     }
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (ws != nullptr) {
-        const cudaError_t ef = workspace_free(ws, stream);
+    for (void *owned : {ws, sync_owned}) {
+        if (owned == nullptr) continue;
+        const cudaError_t ef = workspace_free(owned, stream);
         if (e == cudaSuccess) e = ef;
     }
     return e;

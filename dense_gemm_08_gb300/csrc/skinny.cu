@@ -441,15 +441,19 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
 
     void *ws = nullptr;
+    void *sync_owned = nullptr;  // counters of a captured launch (see split_sync)
     if (a.n_slices > 1) {
         // partial sums from the pool; counters from the stream's split
         // counters (zero; the last slice of a column block resets its own)
         cudaError_t e = split_sync(stream, static_cast<size_t>(a.n_cb), 0, &a.ws_count, nullptr,
-                                   nullptr);
+                                   nullptr, &sync_owned);
         if (e != cudaSuccess) return e;
         const size_t part = static_cast<size_t>(a.n_slices) * p.M * p.N * sizeof(float);
         e = workspace_alloc(part, stream, &ws);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            if (sync_owned != nullptr) workspace_free(sync_owned, stream);
+            return e;
+        }
         a.ws = static_cast<float *>(ws);
     }
     const unsigned g = static_cast<unsigned>(grid);
@@ -464,8 +468,9 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
         *name = p.b_kmajor ? "skinny<bf16,B:K>" : "skinny<bf16,B:N>";
     }
     cudaError_t e = cudaGetLastError();
-    if (ws != nullptr) {
-        const cudaError_t ef = workspace_free(ws, stream);
+    for (void *owned : {ws, sync_owned}) {
+        if (owned == nullptr) continue;
+        const cudaError_t ef = workspace_free(owned, stream);
         if (e == cudaSuccess) e = ef;
     }
     return e;

@@ -20,6 +20,7 @@
 #include <cstdint>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "internal.h"
 
@@ -59,9 +60,14 @@ cudaError_t device_pool(cudaMemPool_t *out) {
 }  // namespace
 
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr) {
-    cudaMemPool_t pool = nullptr;
-    const cudaError_t e = device_pool(&pool);
+    // under stream capture the allocation becomes a graph memory node, which
+    // comes from the graph's own memory, not from a pool of the library
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &capture);
     if (e != cudaSuccess) return e;
+    if (capture != cudaStreamCaptureStatusNone) return cudaMallocAsync(ptr, bytes, stream);
+    cudaMemPool_t pool = nullptr;
+    if ((e = device_pool(&pool)) != cudaSuccess) return e;
     return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
 }
 
@@ -77,27 +83,29 @@ struct SyncBuf {
 };
 std::mutex g_sync_mutex;
 std::unordered_map<uint64_t, SyncBuf> g_sync;  // key: (device, stream)
+std::vector<void *> g_sync_retired;            // outgrown buffers, never freed
 
 uint64_t sync_key(int dev, cudaStream_t stream) {
     return (static_cast<uint64_t>(dev) << 56) ^ reinterpret_cast<uintptr_t>(stream);
 }
 
-// A zeroed buffer of at least `want` words for one of the regions (grown in
-// stream order: the old one is freed after the work already queued on it).
+// A zeroed buffer of at least `want` words for one of the regions.  An
+// outgrown buffer is kept allocated: a launch enqueued by another host thread
+// may still hold its address.
 template <typename T>
 cudaError_t ensure(T **ptr, size_t *have, size_t want, cudaStream_t stream) {
     if (*have >= want) return cudaSuccess;
     size_t n = *have ? *have : 4096;
     while (n < want) n *= 2;
     void *fresh = nullptr;
-    cudaError_t e = workspace_alloc(n * sizeof(T), stream, &fresh);
+    cudaError_t e = cudaMalloc(&fresh, n * sizeof(T));
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(fresh, 0, n * sizeof(T), stream);
     if (e != cudaSuccess) {
-        workspace_free(fresh, stream);
+        cudaFree(fresh);
         return e;
     }
-    if (*ptr != nullptr) workspace_free(*ptr, stream);
+    if (*ptr != nullptr) g_sync_retired.push_back(*ptr);
     *ptr = static_cast<T *>(fresh);
     *have = n;
     return cudaSuccess;
@@ -105,10 +113,29 @@ cudaError_t ensure(T **ptr, size_t *have, size_t want, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t split_sync(cudaStream_t stream, size_t n_counters, size_t n_flags, int **counters,
-                       unsigned **flags, unsigned *generation) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+                       unsigned **flags, unsigned *generation, void **owned) {
+    *owned = nullptr;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &capture);
     if (e != cudaSuccess) return e;
+    if (capture != cudaStreamCaptureStatusNone) {
+        // one zeroed block per captured launch: [counters][flags]
+        const size_t c_bytes = (n_counters * sizeof(int) + 15) & ~static_cast<size_t>(15);
+        const size_t bytes = c_bytes + n_flags * sizeof(unsigned);
+        void *blk = nullptr;
+        if ((e = workspace_alloc(bytes > 0 ? bytes : 16, stream, &blk)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(blk, 0, bytes > 0 ? bytes : 16, stream)) != cudaSuccess) {
+            workspace_free(blk, stream);
+            return e;
+        }
+        *owned = blk;
+        if (counters) *counters = static_cast<int *>(blk);
+        if (flags) *flags = reinterpret_cast<unsigned *>(static_cast<char *>(blk) + c_bytes);
+        if (generation) *generation = 1;
+        return cudaSuccess;
+    }
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_sync_mutex);
     SyncBuf &b = g_sync[sync_key(dev, stream)];
     if ((e = ensure(&b.counters, &b.n_counters, n_counters, stream)) != cudaSuccess) return e;

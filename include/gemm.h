@@ -24,14 +24,21 @@
  * -------------------------------------------------
  * Ownership: A, B, C and D are device pointers owned by the caller (for
  *   example torch CUDA tensors).  The library keeps no pointer after the call
- *   returns; tensor maps travel by value in the launch parameters.  When the
- *   CUDA-core kernel splits the K range of its last tiles across CTAs (to keep
- *   every SM busy), it takes a temporary workspace for partial sums (a few
- *   tens of MiB at most) from a memory pool the library owns, one per device,
- *   allocated and freed in stream order on `stream`; the pool keeps up to
- *   256 MiB of freed memory for later calls.  Nothing else is allocated.  The
- *   library holds no per-call state and may be called from several host
- *   threads.
+ *   returns; tensor maps travel by value in the launch parameters.
+ *   Workspace: a kernel may split the K range of some tiles across CTAs (to
+ *   keep every SM busy).  Such a kernel takes a temporary workspace for the
+ *   partial sums (a few tens of MiB at most) from a memory pool the library
+ *   owns, one per device, allocated and freed in stream order on `stream`.
+ *   The pool keeps up to 256 MiB of freed memory for later calls.  The split
+ *   pieces count themselves in small counters (a few KiB) that the library
+ *   keeps per (device, stream) and that every kernel returns to zero, so no
+ *   call clears them.
+ *   Graph capture: while `stream` is being captured, each call takes fresh
+ *   counters and workspace as graph memory.  The graph may therefore be
+ *   replayed on any stream, beside other calls.
+ *   Threads: calls may come from several host threads.  Calls on one stream
+ *   must not be made from two threads at once: like the stream's own order,
+ *   the counters assume that calls on a stream run one after another.
  * Asynchrony: the work is enqueued on `stream` (0 = the legacy default
  *   stream) and the call returns without waiting for it.  The caller keeps
  *   the buffers alive until the stream has passed the call.

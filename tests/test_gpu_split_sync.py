@@ -4,10 +4,11 @@ Every kernel that splits a tile's K range (tensor-core split-K, the CTA-pair
 kernel's split last round, the CUDA-core stream-K tail, the small-M kernel's
 K slices) counts the finished pieces in counters that belong to the stream
 and persist between calls; the piece that completes a count returns it to
-zero, so no call clears them.  These tests check that calls of every variant,
-back to back in any order, on two streams at once, and after a kernel gave up
-a bounded wait, give the same bits as a first call that is checked against
-the oracle."""
+zero, so no call clears them (a captured call takes fresh zeroed counters
+instead).  These tests check that calls of every variant -- back to back in
+any order, on two streams at once, after a kernel gave up a bounded wait, and
+replayed from a captured graph beside eager calls -- give the same bits as a
+first call that is checked against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -113,3 +114,28 @@ def test_split_variants_after_a_wait_gave_up(cases):
     assert lib.gemm_last_device_status() == lib.GEMM_OK
     for i, D in got:
         assert torch.equal(D, first[i]), cases[i].w.name
+
+
+def test_captured_graph_replays_beside_eager_calls(cases):
+    """A graph captured with every split variant gets its own zeroed counters
+    per captured launch, so replaying it -- here on a side stream while eager
+    calls of the same variants run on the default stream -- gives the same
+    bits as eager calls, replay after replay."""
+    first = _first_results(cases)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = [c.launch() for c in cases]
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        for D in captured:
+            D.zero_()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            graph.replay()
+        eager = [c.launch() for c in cases]
+        torch.cuda.synchronize()
+        assert lib.gemm_last_device_status() == lib.GEMM_OK
+        for i, D in enumerate(captured):
+            assert torch.equal(D, first[i]), cases[i].w.name
+        for i, D in enumerate(eager):
+            assert torch.equal(D, first[i]), cases[i].w.name
