@@ -38,6 +38,7 @@ KERNEL_SOURCES = {
     "gemm_bf16_tc": "dense_gemm_08_gb300/csrc/gemm_tc.cu",
     "gemm_f16_tc": "dense_gemm_08_gb300/csrc/gemm_tc.cu",
     "sgemm_simt": "dense_gemm_08_gb300/csrc/sgemm_simt.cu",
+    "sgemm_cluster": "dense_gemm_08_gb300/csrc/sgemm_cluster.cu",
     "skinny": "dense_gemm_08_gb300/csrc/skinny.cu",
 }
 

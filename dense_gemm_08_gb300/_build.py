@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libdense_gemm_08_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["gemm_api.cu", "sgemm_simt.cu", "gemm_tc.cu", "workspace.cu", "probe.cu", "skinny.cu"]
+SOURCES = ["gemm_api.cu", "sgemm_simt.cu", "sgemm_cluster.cu", "gemm_tc.cu", "workspace.cu",
+           "probe.cu", "skinny.cu"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "epilogue.cuh"),
            os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "gemm_probe.h")]
 

@@ -60,6 +60,14 @@ cudaError_t split_sync_reset_device();
 cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name);
 cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **name);
 
+// FP32 problems with few 64 x 64 tiles: each tile's K range split over the
+// CTAs of a cluster and reduced through distributed shared memory
+// (sgemm_cluster.cu).  sgemm_cluster_size returns the cluster size (2, 4 or
+// 8) to use for `p` on a GPU of `sms` SMs, or 0 when the kernel does not fit.
+int sgemm_cluster_size(const Problem &p, int sms);
+cudaError_t launch_sgemm_cluster(const Problem &p, int cl, cudaStream_t stream,
+                                 const char **name);
+
 // FP32 CUDA-core path whose split-tile workspace is a fixed file-scope device
 // array of kFixedScratchBytes instead of pool memory (nothing is allocated).
 constexpr size_t kFixedScratchBytes = size_t(32) << 20;

@@ -682,7 +682,12 @@ cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const 
     const int64_t sms = sm_count();
     const bool big = tiles(BigCfg::BM, BigCfg::BN) >= sms;
     if (in == InType::F32) {
-        // FP32: a D of at most 64 columns takes 256 x 64 tiles; 128 x 256
+        // FP32 with few 64 x 64 tiles and a K that splits into 2-8 short
+        // slices: the cluster kernel (its pieces add up in shared memory,
+        // not through a global-memory workspace).
+        const int cl = sgemm_cluster_size(p, static_cast<int>(sms));
+        if (cl > 0) return launch_sgemm_cluster(p, cl, stream, name);
+        // Otherwise a D of at most 64 columns takes 256 x 64 tiles; 128 x 256
         // tiles when there are two waves of them and K is long enough to
         // carry their epilogue; else 128 x 128 tiles if there are enough of
         // them for the stream-K tail to spread; else 64 x 64.

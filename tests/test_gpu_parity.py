@@ -53,7 +53,7 @@ def sampled_check(w, inp, rows, cols, n_random=4000, seed=0):
 # ---------------------------------------------------------------- the configs
 def test_f32_256_full():
     w = WORKLOADS["f32_256"]
-    full_check(w, make_inputs(w), pad_d=3, expect_kernel="sgemm_simt<f32")
+    full_check(w, make_inputs(w), pad_d=3, expect_kernel="sgemm_cluster<f32")
 
 
 def test_f32_256_small_integers_bit_exact():
@@ -94,7 +94,7 @@ def test_all_orders_full(dtype, orders):
     M, N, K = MODERATE
     w = Workload(f"mod_{dtype}", M, N, K, 1.5, -0.25, dtype, *orders)
     inp = make_inputs(w, seed=1, pad=3, ld_multiple=8)
-    expect = {"f32": "sgemm_simt<f32", "bf16": "gemm_bf16_tc", "f16": "gemm_f16_tc"}[dtype]
+    expect = {"f32": "sgemm_cluster<f32", "bf16": "gemm_bf16_tc", "f16": "gemm_f16_tc"}[dtype]
     full_check(w, inp, pad_d=5, expect_kernel=expect)
 
 
@@ -393,10 +393,10 @@ def test_tma_store_edges_stay_inside_d(n):
 
 
 # FP32 tile configurations: 128 x 256 (two waves, long K), 128 x 128 (few
-# big tiles or short K), 256 x 64 (D at most 64 wide), 64 x 64 (small);
-# ragged edges and stream-K tails in each.
-SIMT_CFG_SHAPES = [(2560, 5120, 2048), (1100, 1300, 700), (700, 900, 500), (1000, 64, 777),
-                   (3000, 33, 300), (130, 140, 150)]
+# big tiles or short K), 256 x 64 (D at most 64 wide), 64 x 64 (small, K
+# too long for the cluster kernel); ragged edges and stream-K tails in each.
+SIMT_CFG_SHAPES = [(2560, 5120, 2048), (1100, 1300, 700), (700, 900, 500), (2000, 64, 777),
+                   (3000, 33, 300), (130, 140, 1500)]
 
 
 @pytest.mark.parametrize("shape", SIMT_CFG_SHAPES)
