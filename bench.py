@@ -315,7 +315,8 @@ def bench_ours(args):
         # host takes to enqueue the timed steps: the steps then run back to
         # back and the events time the GPU, not the host's call overhead
         # (about 15 us per call through the Python binding).
-        torch.cuda._sleep(int(min(2.0, 2.0 * args.steps * t_host) * SLEEP_CYCLES_PER_S))
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(min(2.0, 2.0 * args.steps * t_host) * SLEEP_CYCLES_PER_S))
         e0.record(stream)
         for _ in range(args.steps):
             kernel_names.add(step())

@@ -30,9 +30,10 @@
  *   partial sums (a few tens of MiB at most) from a memory pool the library
  *   owns, one per device, allocated and freed in stream order on `stream`.
  *   The pool keeps up to 256 MiB of freed memory for later calls.  The split
- *   pieces count themselves in small counters (a few KiB) that the library
- *   keeps per (device, stream) and that every kernel returns to zero, so no
- *   call clears them.
+ *   pieces count themselves in small counters that the library keeps per
+ *   (device, stream) and that every kernel returns to zero, so no call
+ *   clears them.  These take 32 KiB per stream at first (more only for
+ *   problems with more split tiles) and are kept until the process ends.
  *   Graph capture: while `stream` is being captured, each call takes fresh
  *   counters and workspace as graph memory.  The graph may therefore be
  *   replayed on any stream, beside other calls.
