@@ -95,6 +95,15 @@ def source_digest(rel_path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def rotation_copies(working_set, l2_bytes):
+    """How many copies of a step's working set the timed steps rotate over so
+    that each step reads operands not in L2: 1 if the set alone is at least
+    twice L2, else enough copies to exceed twice L2."""
+    if working_set >= 2 * l2_bytes:
+        return 1
+    return -(-2 * l2_bytes // max(working_set, 1))
+
+
 def committed_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, or None if there is none or the kernel source changed since."""
@@ -281,9 +290,7 @@ def bench_ours(args):
     # L2 is copied until the copies exceed it, and step i uses copy i mod n,
     # so every step reads operands that at least 2 x L2 of other data has
     # passed through L2 since their last use.  All copies hold the same values.
-    n_rot = 1
-    if working_set < 2 * L2_BYTES:
-        n_rot = -(-2 * L2_BYTES // working_set)
+    n_rot = rotation_copies(working_set, L2_BYTES)
     rot = [(A, B, C, D)]
     for _ in range(n_rot - 1):
         rot.append((A.clone(), B.clone(), C.clone() if C is not None else None,

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -199,6 +200,35 @@ cudaError_t launch_layout(const ClusterArgs &a, unsigned grid, cudaStream_t stre
     return cudaLaunchKernelEx(&cfg, sgemm_cluster_kernel<CL, AK, BKM>, a);
 }
 
+// Whether the current device can hold at least one cluster of CL CTAs of
+// this kernel at a time (asked once per device and cluster size).
+template <int CL>
+bool cluster_fits() {
+    constexpr int kMaxDevices = 64;
+    static std::once_flag once[kMaxDevices];
+    static bool fits[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::call_once(once[dev], [dev] {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CL, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = CL;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const cudaError_t e =
+            cudaOccupancyMaxActiveClusters(&n, sgemm_cluster_kernel<CL, true, false>, &cfg);
+        fits[dev] = e == cudaSuccess && n > 0;
+        if (e != cudaSuccess) cudaGetLastError();  // a refused query is not a launch error
+    });
+    return fits[dev];
+}
+
 template <int CL>
 cudaError_t launch_cl(const ClusterArgs &a, bool ak, bool bk, unsigned grid, cudaStream_t stream) {
     if (ak && bk) return launch_layout<CL, true, true>(a, grid, stream);
@@ -213,11 +243,14 @@ int sgemm_cluster_size(const Problem &p, int sms) {
     if (p.M < 1 || p.N < 1 || p.K < 1) return 0;
     const int64_t tiles = ((p.M + kTile - 1) / kTile) * ((p.N + kTile - 1) / kTile);
     // the most K pieces per tile with one CTA per SM, every piece at least
-    // one chunk long and at most kMaxChunksPerSlice chunks
+    // one chunk long and at most kMaxChunksPerSlice chunks, in clusters the
+    // device can schedule
     for (int cl = 8; cl >= 2; cl /= 2) {
         if (tiles * cl > sms) continue;
         if (p.K < static_cast<int64_t>(cl) * kChunk) continue;
         if (p.K > static_cast<int64_t>(cl) * kChunk * kMaxChunksPerSlice) continue;
+        const bool fits = cl == 8 ? cluster_fits<8>() : cl == 4 ? cluster_fits<4>() : cluster_fits<2>();
+        if (!fits) continue;
         return cl;
     }
     return 0;

@@ -115,3 +115,15 @@ def test_max_over_ranks_with_two_gloo_ranks():
         p.join(timeout=120)
         assert p.exitcode == 0
     assert dict(out) == {0: 7.25, 1: 7.25}
+
+
+def test_rotation_copies_exceed_twice_l2():
+    l2 = bench.L2_BYTES
+    # FP32 256^3: A, B and D of 256 KiB each
+    ws = 3 * 256 * 256 * 4
+    n = bench.rotation_copies(ws, l2)
+    assert n * ws >= 2 * l2 and (n - 1) * ws < 2 * l2
+    # FP32 4096^3 (192 MiB) needs two copies; BF16 8192^3 (512 MiB) needs none
+    assert bench.rotation_copies(192 * 2**20, l2) == 2
+    assert bench.rotation_copies(512 * 2**20, l2) == 1
+    assert bench.rotation_copies(2 * l2, l2) == 1
