@@ -139,3 +139,39 @@ def test_captured_graph_replays_beside_eager_calls(cases):
             assert torch.equal(D, first[i]), cases[i].w.name
         for i, D in enumerate(eager):
             assert torch.equal(D, first[i]), cases[i].w.name
+
+
+def test_host_threads_on_their_own_streams(cases):
+    """Four host threads, each on its own stream, call every split variant at
+    the same time (the binding releases the GIL during a call): each stream
+    has its own counters, so every result matches the first call."""
+    import threading
+    first = _first_results(cases)
+    got, errors = {}, []
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            out = []
+            with torch.cuda.stream(s):
+                for rep in range(3):
+                    for i in range(len(cases)):
+                        j = (i + t + rep) % len(cases)
+                        out.append((j, cases[j].launch(s)))
+            s.synchronize()
+            got[t] = out
+        except Exception as e:  # surfaced below, in the test's thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    for t, out in got.items():
+        for i, D in out:
+            assert torch.equal(D, first[i]), (t, cases[i].w.name)
