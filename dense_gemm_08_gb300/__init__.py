@@ -9,6 +9,7 @@ first call (there is no CPU fallback).
 Same names as the C ABI:
     gemm_f32, gemm_bf16_f32acc, gemm_f16_f32acc, gemm_bf16_f32acc_ex,
     gemm_f32_noalloc, gemm_status_string, gemm_last_device_status, gemm_last_kernel,
+    gemm_memory_info, gemm_release_memory,
     gemm_probe_tc_bf16, gemm_probe_fma_f32, gemm_probe_wait_timeout
 Pointer arguments take an integer device address or a torch CUDA tensor;
 ``stream`` takes an integer ``cudaStream_t``, a ``torch.cuda.Stream`` or None
@@ -36,14 +37,20 @@ GEMM_ERR_INTERNAL = 5
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
 EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_bf16_f32acc_ex",
             "gemm_f32_noalloc", "gemm_status_string", "gemm_last_device_status",
-            "gemm_last_kernel", "gemm_probe_tc_bf16", "gemm_probe_fma_f32",
-            "gemm_probe_wait_timeout")
+            "gemm_last_kernel", "gemm_memory_info", "gemm_release_memory",
+            "gemm_probe_tc_bf16", "gemm_probe_fma_f32", "gemm_probe_wait_timeout")
 
 GEMM_ACT_NONE = 0
 GEMM_ACT_RELU = 1
 GEMM_ACT_GELU = 2
 GEMM_D_F32 = 0
 GEMM_D_BF16 = 1
+
+
+class MemoryInfo(ctypes.Structure):
+    """gemm_memory_info_t: what the library holds on the current device."""
+    _fields_ = [("split_streams", ctypes.c_uint64), ("split_bytes", ctypes.c_uint64),
+                ("pool_used_bytes", ctypes.c_uint64), ("pool_reserved_bytes", ctypes.c_uint64)]
 
 
 class Epilogue(ctypes.Structure):
@@ -88,6 +95,10 @@ def library() -> ctypes.CDLL:
             lib.gemm_last_device_status.restype = ip
             lib.gemm_last_kernel.argtypes = []
             lib.gemm_last_kernel.restype = ctypes.c_char_p
+            lib.gemm_memory_info.argtypes = [ctypes.POINTER(MemoryInfo)]
+            lib.gemm_memory_info.restype = ip
+            lib.gemm_release_memory.argtypes = []
+            lib.gemm_release_memory.restype = ip
             dp = ctypes.POINTER(ctypes.c_double)
             lib.gemm_probe_tc_bf16.argtypes = [ip, i64, dp, vp]
             lib.gemm_probe_tc_bf16.restype = ip
@@ -181,6 +192,23 @@ def gemm_last_device_status(stream=None) -> int:
 
 def gemm_last_kernel() -> str:
     return library().gemm_last_kernel().decode()
+
+
+def gemm_memory_info(check=True) -> dict:
+    """What the library holds on the current device between calls (see include/gemm.h)."""
+    info = MemoryInfo()
+    st = library().gemm_memory_info(ctypes.byref(info))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_memory_info")
+    return {name: int(getattr(info, name)) for name, _ in MemoryInfo._fields_}
+
+
+def gemm_release_memory(check=True) -> int:
+    """Synchronise the device, free every stream's split counters and trim the pool."""
+    st = int(library().gemm_release_memory())
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_release_memory")
+    return st
 
 
 def gemm_probe_tc_bf16(cta_group, n_mma, stream=None, check=True):

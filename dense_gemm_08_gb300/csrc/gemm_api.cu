@@ -128,10 +128,8 @@ GEMM_API gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, co
     cudaError_t e;
     if (K == 0 || alpha == 0.f)
         e = gemm::launch_scale_c(p, stream, &name);
-    else if (gemm::skinny_eligible(p))
-        e = gemm::launch_skinny(p, gemm::InType::F32, stream, &name);
     else
-        e = gemm::launch_simt(p, gemm::InType::F32, stream, &name);
+        e = gemm::launch_f32(p, stream, &name);
     return finish(e, name);
 }
 
@@ -242,10 +240,16 @@ GEMM_API gemm_status_t gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, float a
     if (K == 0 || alpha == 0.f) {
         e = gemm::launch_scale_c(p, stream, &name);
     } else {
-        // the split-tile workspace must fit the fixed array: refuse before any launch
-        if (gemm::simt_f32_scratch_bytes(p) > gemm::kFixedScratchBytes)
+        // gemm_f32's kernel and work split, with its split pieces in the
+        // fixed array: refuse before anything is enqueued if they do not fit
+        size_t part = 0, counters = 0;
+        gemm::f32_scratch_needs(p, &part, &counters);
+        if (part > gemm::kFixedScratchBytes - gemm::kFixedCounterBytes ||
+            counters > gemm::kFixedCounterBytes / sizeof(int))
             return GEMM_ERR_INVALID_VALUE;
-        e = gemm::launch_simt_fixed_scratch(p, stream, &name);
+        gemm::FixedScratch fixed{};
+        if (gemm::fixed_scratch(&fixed, stream) != cudaSuccess) return GEMM_ERR_INTERNAL;
+        e = gemm::launch_f32(p, stream, &name, &fixed);
     }
     return finish(e, name);
 }
@@ -267,10 +271,30 @@ GEMM_API gemm_status_t gemm_last_device_status(cudaStream_t stream) {
     if (gemm::tc_read_and_clear_status(stream, &status) != cudaSuccess) return GEMM_ERR_INTERNAL;
     if (status) {
         // a kernel that gave up may have left split counters mid-count
-        if (gemm::split_sync_reset_device() != cudaSuccess) return GEMM_ERR_INTERNAL;
+        if (gemm::split_sync_release_device() != cudaSuccess) return GEMM_ERR_INTERNAL;
         return GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_memory_info(gemm_memory_info_t *info) {
+    if (info == nullptr) return GEMM_ERR_INVALID_VALUE;
+    *info = gemm_memory_info_t{0, 0, 0, 0};
+    const gemm_status_t dev = check_device();
+    if (dev != GEMM_OK) return dev;
+    gemm::MemoryInfo m;
+    if (gemm::memory_info(&m) != cudaSuccess) return GEMM_ERR_INTERNAL;
+    info->split_streams = m.split_streams;
+    info->split_bytes = m.split_bytes;
+    info->pool_used_bytes = m.pool_used_bytes;
+    info->pool_reserved_bytes = m.pool_reserved_bytes;
+    return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_release_memory(void) {
+    const gemm_status_t dev = check_device();
+    if (dev != GEMM_OK) return dev;
+    return gemm::release_memory() == cudaSuccess ? GEMM_OK : GEMM_ERR_INTERNAL;
 }
 
 GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }

@@ -1414,28 +1414,26 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         a.tail_first = tail_ks > 1 ? pair_tiles - tail : pair_tiles;
         a.tail_ks = static_cast<int>(tail_ks);
         void *ws = nullptr;
-        void *sync_owned = nullptr;  // counters of a captured launch (see split_sync)
+        SplitSync sync;  // the stream's split counters, held until the launch is enqueued
         if (tail_ks > 1) {
             *name = bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>";
             // counters: per tail tile 2 CTAs x 4 warps (the stream's, zero)
-            e = split_sync(stream, static_cast<size_t>(tail) * 2 * 4, 0, &a.ws_count, nullptr,
-                           nullptr, &sync_owned);
+            e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * 4, 0);
             if (e != cudaSuccess) return e;
+            a.ws_count = sync.counters;
             // per tail tile and piece: 2 CTAs x 4 warps x 8 boxes of 4 KiB
             const size_t part_bytes = static_cast<size_t>(tail) * tail_ks * 2 * 4 * 8 * 4096;
             e = workspace_alloc(part_bytes, stream, &ws);
-            if (e != cudaSuccess) {
-                if (sync_owned != nullptr) workspace_free(sync_owned, stream);
-                return e;
-            }
+            if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
         }
         e = launch_variant<2>(p, a, 2 * d->pairs, stream);
-        for (void *owned : {ws, sync_owned}) {
-            if (owned == nullptr) continue;
-            const cudaError_t ef = workspace_free(owned, stream);
+        if (ws != nullptr) {
+            const cudaError_t ef = workspace_free(ws, stream);
             if (e == cudaSuccess) e = ef;
         }
+        const cudaError_t er = sync.release();
+        if (e == cudaSuccess) e = er;
     } else {
         const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
         // Fewer tiles than SMs: split each tile's K range over ks CTAs
@@ -1451,19 +1449,18 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             if (ks < 2) ks = 1;
         }
         void *ws = nullptr;
-        void *sync_owned = nullptr;  // counters and flags of a captured launch
+        SplitSync sync;  // the stream's split counters and flags, held until enqueued
         if (ks > 1) {
             // counters and flags: per tile 4 warps (the stream's: counters
-            // zero, flags below this call's generation)
-            e = split_sync(stream, static_cast<size_t>(tiles) * 4, static_cast<size_t>(tiles) * 4,
-                           &a.ws_count, &a.ws_flag, &a.generation, &sync_owned);
+            // zero, flags other than this call's generation)
+            e = sync.acquire(stream, static_cast<size_t>(tiles) * 4, static_cast<size_t>(tiles) * 4);
             if (e != cudaSuccess) return e;
+            a.ws_count = sync.counters;
+            a.ws_flag = sync.flags;
+            a.generation = sync.generation;
             const size_t part_bytes = static_cast<size_t>(tiles) * ks * 4 * 8 * 4096;
             e = workspace_alloc(part_bytes, stream, &ws);
-            if (e != cudaSuccess) {
-                if (sync_owned != nullptr) workspace_free(sync_owned, stream);
-                return e;
-            }
+            if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
             a.ks = static_cast<int>(ks);
             *name = bf16 ? "gemm_bf16_tc<splitk>" : "gemm_f16_tc<splitk>";
@@ -1473,11 +1470,12 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         const int64_t items = tiles * ks;
         const int grid = static_cast<int>(items < d->sms ? items : d->sms);
         e = launch_variant<1>(p, a, grid, stream);
-        for (void *owned : {ws, sync_owned}) {
-            if (owned == nullptr) continue;
-            const cudaError_t ef = workspace_free(owned, stream);
+        if (ws != nullptr) {
+            const cudaError_t ef = workspace_free(ws, stream);
             if (e == cudaSuccess) e = ef;
         }
+        const cudaError_t er = sync.release();
+        if (e == cudaSuccess) e = er;
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

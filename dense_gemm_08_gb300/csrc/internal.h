@@ -6,6 +6,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 namespace gemm {
@@ -39,21 +41,52 @@ enum class InType { F32, BF16, F16 };
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr);
 cudaError_t workspace_free(void *ptr, cudaStream_t stream);
 // The split kernels' counters and flags for one launch on `stream` (current
-// device): at least n_counters ints that are zero and n_flags unsigned flags
-// that are below *generation, the number this launch writes to a flag.
-//   Eager calls get the stream's persistent buffers and enqueue nothing:
-//   every kernel returns the counters it used to zero, and calls on one
-//   stream run in order, so they may share them (calls on other streams
-//   have their own).  *owned = nullptr.
+// device): after acquire, `counters` has at least n_counters ints that are
+// zero and `flags` at least n_flags unsigned flags that differ from
+// `generation`, the number this launch writes to a flag.
+//   Eager calls get the stream's persistent buffers and enqueue nothing
+//   (except when the buffers grow): every kernel returns the counters it used
+//   to zero, and calls on one stream run in order, so they may share them
+//   (other streams have their own).  The stream's entry stays held until
+//   release(), which the caller invokes once its launch is enqueued; so the
+//   launches of one stream are enqueued in generation order, from any number
+//   of host threads.
 //   Under stream capture a graph may be replayed on any stream, at the same
 //   time as other work, with the generation fixed at capture: the call gets a
-//   fresh zeroed block from the pool instead (*owned = its address, generation
-//   1), which the caller frees in stream order after its launch.
-cudaError_t split_sync(cudaStream_t stream, size_t n_counters, size_t n_flags, int **counters,
-                       unsigned **flags, unsigned *generation, void **owned);
-// After a bounded wait ran out (counters may be left mid-count): zero every
-// stream's counters and flags of the current device (synchronises the device).
-cudaError_t split_sync_reset_device();
+//   fresh zeroed block of graph memory instead (generation 1), freed in
+//   stream order by release().
+class SplitSync {
+   public:
+    SplitSync() = default;
+    SplitSync(const SplitSync &) = delete;
+    SplitSync &operator=(const SplitSync &) = delete;
+    ~SplitSync();
+    cudaError_t acquire(cudaStream_t stream, size_t n_counters, size_t n_flags);
+    cudaError_t release();
+    int *counters = nullptr;
+    unsigned *flags = nullptr;
+    unsigned generation = 0;
+
+   private:
+    cudaStream_t stream_ = nullptr;
+    void *owned_ = nullptr;              // captured launch: its block
+    std::unique_lock<std::mutex> lock_;  // eager launch: the stream's entry
+};
+// Frees every stream's split counters and flags on the current device after
+// synchronising it (the next split call on a stream creates zeroed ones).
+// Used after a bounded wait ran out, when counters may be left mid-count.
+cudaError_t split_sync_release_device();
+
+// What the library holds on the current device between calls.
+struct MemoryInfo {
+    uint64_t split_streams = 0;        // streams with split counters
+    uint64_t split_bytes = 0;          // bytes of those counters and flags
+    uint64_t pool_used_bytes = 0;      // pool memory in use (counters, pending workspace)
+    uint64_t pool_reserved_bytes = 0;  // pool memory held from the driver
+};
+cudaError_t memory_info(MemoryInfo *out);
+// split_sync_release_device, then the pool returns all its free memory.
+cudaError_t release_memory();
 
 // Each launcher enqueues one kernel on `stream`, returns the CUDA error of
 // the launch and sets *name to the kernel's static name.
@@ -68,12 +101,34 @@ int sgemm_cluster_size(const Problem &p, int sms);
 cudaError_t launch_sgemm_cluster(const Problem &p, int cl, cudaStream_t stream,
                                  const char **name);
 
-// FP32 CUDA-core path whose split-tile workspace is a fixed file-scope device
-// array of kFixedScratchBytes instead of pool memory (nothing is allocated).
+// Scratch supplied in place of pool memory (gemm_f32_noalloc): `counters`
+// holds n_counters ints that are zero between calls (every kernel returns
+// the counters it used to zero), `part` holds part_bytes for partial sums.
+struct FixedScratch {
+    int *counters;
+    size_t n_counters;
+    void *part;
+    size_t part_bytes;
+};
+// The library's fixed scratch array (sgemm_simt.cu): kFixedScratchBytes in
+// all, the first kFixedCounterBytes of it counters, the rest partial sums.
 constexpr size_t kFixedScratchBytes = size_t(32) << 20;
-// Workspace the FP32 CUDA-core path needs for `p` (0 if it splits no tile).
-size_t simt_f32_scratch_bytes(const Problem &p);
-cudaError_t launch_simt_fixed_scratch(const Problem &p, cudaStream_t stream, const char **name);
+constexpr size_t kFixedCounterBytes = size_t(16) << 10;
+// The current device's fixed scratch.  The first call on a device looks up
+// the array's address and zeroes its counters (waiting for that on
+// `stream`); it fails under stream capture.
+cudaError_t fixed_scratch(FixedScratch *out, cudaStream_t stream);
+
+// The FP32 path of gemm_f32 (A, B FP32; K > 0, alpha != 0): the small-M
+// kernel for M <= kSkinnyMaxM, else the cluster kernel where it fits, else
+// the CUDA-core kernel in the tile configuration that suits the shape.
+// With `fixed`, the split pieces use it instead of pool memory and the
+// stream's counters (the same kernel and work split either way).
+cudaError_t launch_f32(const Problem &p, cudaStream_t stream, const char **name,
+                       const FixedScratch *fixed = nullptr);
+// Scratch launch_f32 takes for `p`: partial-sum bytes and counters (both 0
+// when no tile is split).
+void f32_scratch_needs(const Problem &p, size_t *part_bytes, size_t *n_counters);
 
 // Tensor-core (tcgen05) path for BF16 or FP16 inputs.  Returns
 // cudaErrorNotSupported (without launching) when the operands cannot be
@@ -87,7 +142,9 @@ cudaError_t tc_read_and_clear_status(cudaStream_t stream, int *status);
 // normalisation): a kernel that streams op(B) once (skinny.cu).
 constexpr int64_t kSkinnyMaxM = 8;
 bool skinny_eligible(const Problem &p);
-cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, const char **name);
+cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, const char **name,
+                          const FixedScratch *fixed = nullptr);
+void skinny_scratch_needs(const Problem &p, InType in, size_t *part_bytes, size_t *n_counters);
 
 // Peak probes (no memory traffic).  Each enqueues one kernel on `stream` and
 // stores the FLOPs it performs in *flops.

@@ -542,18 +542,17 @@ SplitPlan plan_split(const Problem &p, int64_t tiles) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Caller-supplied scratch for the split tiles (see launch_simt_fixed_scratch).
-struct FixedScratch {
-    void *ptr;
-    size_t bytes;
-};
-
+// Scratch the split plan of config Cfg takes for `p`: partial-sum bytes and
+// counters (one per dealt-out tile).
 template <typename Cfg>
-size_t split_workspace_bytes(const SplitPlan &plan) {
-    if (plan.tail_tiles == 0) return 0;
-    return align256(static_cast<size_t>(plan.tail_tiles) * plan.max_contrib * Cfg::BM * Cfg::BN *
-                    sizeof(float)) +
-           static_cast<size_t>(plan.tail_tiles) * sizeof(int);
+void split_needs(const Problem &p, size_t *part_bytes, size_t *n_counters) {
+    const int64_t tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + Cfg::BN - 1) / Cfg::BN);
+    const SplitPlan plan = plan_split<Cfg>(p, tiles);
+    *part_bytes = plan.tail_tiles == 0
+                      ? 0
+                      : align256(static_cast<size_t>(plan.tail_tiles) * plan.max_contrib *
+                                 Cfg::BM * Cfg::BN * sizeof(float));
+    *n_counters = static_cast<size_t>(plan.tail_tiles);
 }
 
 // Only BF16 inputs reach the fused epilogue (gemm_bf16_f32acc_ex); the other
@@ -597,29 +596,26 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
 
     // workspace for the dealt-out tiles: partial sums, then one counter per tile
     void *ws = nullptr;
-    void *sync_owned = nullptr;  // counters of a captured launch (see split_sync)
+    SplitSync sync;  // the stream's split counters, held until the launch is enqueued
     if (plan.tail_tiles > 0) {
         const size_t part_bytes = align256(static_cast<size_t>(plan.tail_tiles) *
                                            plan.max_contrib * Cfg::BM * Cfg::BN * sizeof(float));
-        const size_t count_bytes = static_cast<size_t>(plan.tail_tiles) * sizeof(int);
         if (fixed != nullptr) {
-            // no allocation: the caller's scratch (its size was checked before)
-            if (part_bytes + count_bytes > fixed->bytes) return cudaErrorInvalidValue;
-            args.ws_part = static_cast<float *>(fixed->ptr);
-            args.ws_count = reinterpret_cast<int *>(static_cast<char *>(fixed->ptr) + part_bytes);
-            const cudaError_t e = cudaMemsetAsync(args.ws_count, 0, count_bytes, stream);
-            if (e != cudaSuccess) return e;
+            // no allocation: the caller's scratch, whose counters are zero
+            // between calls (the last contributor of a tile resets its own)
+            if (part_bytes > fixed->part_bytes ||
+                static_cast<size_t>(plan.tail_tiles) > fixed->n_counters)
+                return cudaErrorInvalidValue;
+            args.ws_part = static_cast<float *>(fixed->part);
+            args.ws_count = fixed->counters;
         } else {
             // partial sums from the pool; counters from the stream's split
             // counters (zero; the last contributor of a tile resets its own)
-            cudaError_t e = split_sync(stream, static_cast<size_t>(plan.tail_tiles), 0,
-                                       &args.ws_count, nullptr, nullptr, &sync_owned);
+            cudaError_t e = sync.acquire(stream, static_cast<size_t>(plan.tail_tiles), 0);
             if (e != cudaSuccess) return e;
+            args.ws_count = sync.counters;
             e = workspace_alloc(part_bytes, stream, &ws);
-            if (e != cudaSuccess) {
-                if (sync_owned != nullptr) workspace_free(sync_owned, stream);
-                return e;
-            }
+            if (e != cudaSuccess) return e;
             args.ws_part = static_cast<float *>(ws);
         }
     }
@@ -649,12 +645,12 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
         *name = names[kind][3];
     }
     if (e == cudaSuccess) e = cudaGetLastError();
-    for (void *owned : {ws, sync_owned}) {
-        if (owned == nullptr) continue;
-        const cudaError_t ef = workspace_free(owned, stream);
+    if (ws != nullptr) {
+        const cudaError_t ef = workspace_free(ws, stream);
         if (e == cudaSuccess) e = ef;
     }
-    return e;
+    const cudaError_t er = sync.release();
+    return e != cudaSuccess ? e : er;
 }
 
 __global__ void scale_c_kernel(const Problem p) {
@@ -675,29 +671,71 @@ __global__ void scale_c_kernel(const Problem p) {
 
 }  // namespace
 
-cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name) {
+namespace {
+// The FP32 kernel choice for K > 0, alpha != 0 (shared by gemm_f32 and
+// gemm_f32_noalloc).
+enum class F32Kernel { Skinny, Cluster, Tall, Big, Wide, Small };
+
+F32Kernel choose_f32(const Problem &p, int *cluster) {
     auto tiles = [&p](int64_t bm, int64_t bn) {
         return ((p.M + bm - 1) / bm) * ((p.N + bn - 1) / bn);
     };
     const int64_t sms = sm_count();
-    const bool big = tiles(BigCfg::BM, BigCfg::BN) >= sms;
-    if (in == InType::F32) {
-        // FP32 with few 64 x 64 tiles and a K that splits into 2-8 short
-        // slices: the cluster kernel (its pieces add up in shared memory,
-        // not through a global-memory workspace).
-        const int cl = sgemm_cluster_size(p, static_cast<int>(sms));
-        if (cl > 0) return launch_sgemm_cluster(p, cl, stream, name);
-        // Otherwise a D of at most 64 columns takes 256 x 64 tiles; 128 x 256
-        // tiles when there are two waves of them and K is long enough to
-        // carry their epilogue; else 128 x 128 tiles if there are enough of
-        // them for the stream-K tail to spread; else 64 x 64.
-        if (p.N <= TallCfg::BN) return launch_cfg<TallCfg, float>(p, stream, name);
-        if (tiles(BigCfg::BM, BigCfg::BN) >= 2 * sms && p.K >= 2048)
-            return launch_cfg<BigCfg, float>(p, stream, name);
-        if (tiles(WideCfg::BM, WideCfg::BN) * 4 >= sms)
-            return launch_cfg<WideCfg, float>(p, stream, name);
-        return launch_cfg<SmallCfg, float>(p, stream, name);
+    *cluster = 0;
+    // M <= 8: the small-M kernel streams op(B) once
+    if (skinny_eligible(p)) return F32Kernel::Skinny;
+    // few 64 x 64 tiles and a K that splits into 2-8 short slices: the
+    // cluster kernel (its pieces add up in shared memory, not through a
+    // global-memory workspace)
+    const int cl = sgemm_cluster_size(p, static_cast<int>(sms));
+    if (cl > 0) {
+        *cluster = cl;
+        return F32Kernel::Cluster;
     }
+    // otherwise a D of at most 64 columns takes 256 x 64 tiles; 128 x 256
+    // tiles when there are two waves of them and K is long enough to carry
+    // their epilogue; else 128 x 128 tiles if there are enough of them for
+    // the stream-K tail to spread; else 64 x 64
+    if (p.N <= TallCfg::BN) return F32Kernel::Tall;
+    if (tiles(BigCfg::BM, BigCfg::BN) >= 2 * sms && p.K >= 2048) return F32Kernel::Big;
+    if (tiles(WideCfg::BM, WideCfg::BN) * 4 >= sms) return F32Kernel::Wide;
+    return F32Kernel::Small;
+}
+}  // namespace
+
+cudaError_t launch_f32(const Problem &p, cudaStream_t stream, const char **name,
+                       const FixedScratch *fixed) {
+    int cl = 0;
+    switch (choose_f32(p, &cl)) {
+        case F32Kernel::Skinny: return launch_skinny(p, InType::F32, stream, name, fixed);
+        case F32Kernel::Cluster: return launch_sgemm_cluster(p, cl, stream, name);
+        case F32Kernel::Tall: return launch_cfg<TallCfg, float>(p, stream, name, fixed);
+        case F32Kernel::Big: return launch_cfg<BigCfg, float>(p, stream, name, fixed);
+        case F32Kernel::Wide: return launch_cfg<WideCfg, float>(p, stream, name, fixed);
+        case F32Kernel::Small: break;
+    }
+    return launch_cfg<SmallCfg, float>(p, stream, name, fixed);
+}
+
+void f32_scratch_needs(const Problem &p, size_t *part_bytes, size_t *n_counters) {
+    int cl = 0;
+    *part_bytes = 0;
+    *n_counters = 0;
+    switch (choose_f32(p, &cl)) {
+        case F32Kernel::Skinny: skinny_scratch_needs(p, InType::F32, part_bytes, n_counters); return;
+        case F32Kernel::Cluster: return;  // pieces meet in distributed shared memory
+        case F32Kernel::Tall: split_needs<TallCfg>(p, part_bytes, n_counters); return;
+        case F32Kernel::Big: split_needs<BigCfg>(p, part_bytes, n_counters); return;
+        case F32Kernel::Wide: split_needs<WideCfg>(p, part_bytes, n_counters); return;
+        case F32Kernel::Small: break;
+    }
+    split_needs<SmallCfg>(p, part_bytes, n_counters);
+}
+
+cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const char **name) {
+    if (in == InType::F32) return launch_f32(p, stream, name);
+    const bool big = ((p.M + BigCfg::BM - 1) / BigCfg::BM) * ((p.N + BigCfg::BN - 1) / BigCfg::BN) >=
+                     sm_count();
     if (in == InType::F16)
         return big ? launch_cfg<BigCfg, __half>(p, stream, name)
                    : launch_cfg<SmallCfg, __half>(p, stream, name);
@@ -705,63 +743,56 @@ cudaError_t launch_simt(const Problem &p, InType in, cudaStream_t stream, const 
                : launch_cfg<SmallCfg, uint16_t>(p, stream, name);
 }
 
-// ----------------------------------------------------- fixed-scratch variant
-// For callers that cannot allocate device memory: the split-tile workspace
-// lives in this file-scope array instead of the pool.  Every device that
-// loads the library holds it until the process exits.  In host code the name
-// g_fixed_scratch is only a host-side stand-in for the array, not a device
-// address: the device address is looked up per device with
-// cudaGetSymbolAddress (with that device current) and passed to the kernel.
-namespace {
-__device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+// ----------------------------------------------------- fixed scratch array
+// For callers that cannot allocate device memory (gemm_f32_noalloc): the
+// split pieces' counters and partial sums live in this file-scope array
+// instead of pool memory.  Every device that loads the library holds it
+// until the process exits.  In host code the name g_fixed_scratch is only a
+// host-side stand-in for the array, not a device address: the device
+// address is looked up per device with cudaGetSymbolAddress (with that
+// device current) and passed to the kernels.  Layout: kFixedCounterBytes of
+// counters, then partial sums.  The counters are zeroed at set-up, and every
+// kernel that counts on them leaves them at zero (the last piece of a tile
+// resets its counter), so no call clears them.
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 
+namespace {
 constexpr int kMaxScratchDevices = 64;
-struct FixedScratchAddr {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+struct FixedScratchSetup {
+    std::mutex m;
+    bool done = false;
     void *ptr = nullptr;
 };
-FixedScratchAddr g_fixed_addr[kMaxScratchDevices];
+FixedScratchSetup g_fixed_setup[kMaxScratchDevices];
+}  // namespace
 
-// The current device's address of g_fixed_scratch (looked up once per device).
-cudaError_t fixed_scratch_address(void **out) {
+cudaError_t fixed_scratch(FixedScratch *out, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
-    FixedScratchAddr &a = g_fixed_addr[dev];
-    std::call_once(a.once, [&a] {
-        void *ptr = nullptr;
-        a.err = cudaGetSymbolAddress(&ptr, g_fixed_scratch);
-        a.ptr = ptr;
-    });
-    *out = a.ptr;
-    return a.err;
-}
-
-template <typename Cfg>
-size_t needed_for(const Problem &p) {
-    const int64_t tiles = ((p.M + Cfg::BM - 1) / Cfg::BM) * ((p.N + Cfg::BN - 1) / Cfg::BN);
-    return split_workspace_bytes<Cfg>(plan_split<Cfg>(p, tiles));
-}
-
-bool use_big(const Problem &p) {
-    const int64_t big_tiles = ((p.M + BigCfg::BM - 1) / BigCfg::BM) *
-                              ((p.N + BigCfg::BN - 1) / BigCfg::BN);
-    return big_tiles >= sm_count();
-}
-}  // namespace
-
-size_t simt_f32_scratch_bytes(const Problem &p) {
-    return use_big(p) ? needed_for<BigCfg>(p) : needed_for<SmallCfg>(p);
-}
-
-cudaError_t launch_simt_fixed_scratch(const Problem &p, cudaStream_t stream, const char **name) {
-    FixedScratch fixed{nullptr, kFixedScratchBytes};
-    const cudaError_t e = fixed_scratch_address(&fixed.ptr);
-    if (e != cudaSuccess) return e;
-    return use_big(p) ? launch_cfg<BigCfg, float>(p, stream, name, &fixed)
-                      : launch_cfg<SmallCfg, float>(p, stream, name, &fixed);
+    FixedScratchSetup &su = g_fixed_setup[dev];
+    {
+        std::lock_guard<std::mutex> lock(su.m);
+        if (!su.done) {
+            // set-up, once per device with the device current: the array's
+            // device address, and zeroed counters before any kernel uses them
+            cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+            if ((e = cudaStreamIsCapturing(stream, &capture)) != cudaSuccess) return e;
+            if (capture != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
+            void *ptr = nullptr;
+            if ((e = cudaGetSymbolAddress(&ptr, g_fixed_scratch)) != cudaSuccess) return e;
+            if ((e = cudaMemsetAsync(ptr, 0, kFixedCounterBytes, stream)) != cudaSuccess) return e;
+            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+            su.ptr = ptr;
+            su.done = true;
+        }
+    }
+    out->counters = static_cast<int *>(su.ptr);
+    out->n_counters = kFixedCounterBytes / sizeof(int);
+    out->part = static_cast<unsigned char *>(su.ptr) + kFixedCounterBytes;
+    out->part_bytes = kFixedScratchBytes - kFixedCounterBytes;
+    return cudaSuccess;
 }
 
 cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **name) {

@@ -407,8 +407,10 @@ void launch_t(const SkinnyArgs &a, unsigned grid, cudaStream_t stream) {
 bool skinny_eligible(const Problem &p) { return p.M >= 1 && p.M <= kSkinnyMaxM && p.K > 0; }
 
 
-cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, const char **name) {
-    if (!skinny_eligible(p)) return cudaErrorInvalidValue;
+namespace {
+// The launch plan: column blocks, K slices (a.n_cb, a.ks, a.n_slices) and
+// wide-load eligibility for `p`.
+SkinnyArgs plan_skinny(const Problem &p, InType in) {
     const int64_t esz = in == InType::F32 ? 4 : 2;
     SkinnyArgs a;
     a.p = p;
@@ -437,24 +439,48 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
     a.n_slices = static_cast<int>((p.K + ks - 1) / ks);
     a.ws = nullptr;
     a.ws_count = nullptr;
+    return a;
+}
+}  // namespace
+
+void skinny_scratch_needs(const Problem &p, InType in, size_t *part_bytes, size_t *n_counters) {
+    *part_bytes = 0;
+    *n_counters = 0;
+    if (!skinny_eligible(p)) return;
+    const SkinnyArgs a = plan_skinny(p, in);
+    if (a.n_slices <= 1) return;
+    *part_bytes = static_cast<size_t>(a.n_slices) * p.M * p.N * sizeof(float);
+    *n_counters = static_cast<size_t>(a.n_cb);
+}
+
+cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, const char **name,
+                          const FixedScratch *fixed) {
+    if (!skinny_eligible(p)) return cudaErrorInvalidValue;
+    SkinnyArgs a = plan_skinny(p, in);
     const int64_t grid = a.n_cb * a.n_slices;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
 
     void *ws = nullptr;
-    void *sync_owned = nullptr;  // counters of a captured launch (see split_sync)
+    SplitSync sync;  // the stream's split counters, held until the launch is enqueued
     if (a.n_slices > 1) {
-        // partial sums from the pool; counters from the stream's split
-        // counters (zero; the last slice of a column block resets its own)
-        cudaError_t e = split_sync(stream, static_cast<size_t>(a.n_cb), 0, &a.ws_count, nullptr,
-                                   nullptr, &sync_owned);
-        if (e != cudaSuccess) return e;
         const size_t part = static_cast<size_t>(a.n_slices) * p.M * p.N * sizeof(float);
-        e = workspace_alloc(part, stream, &ws);
-        if (e != cudaSuccess) {
-            if (sync_owned != nullptr) workspace_free(sync_owned, stream);
-            return e;
+        if (fixed != nullptr) {
+            // the caller's scratch: counters zero between calls (the last
+            // slice of a column block resets its own)
+            if (part > fixed->part_bytes || static_cast<size_t>(a.n_cb) > fixed->n_counters)
+                return cudaErrorInvalidValue;
+            a.ws_count = fixed->counters;
+            a.ws = static_cast<float *>(fixed->part);
+        } else {
+            // partial sums from the pool; counters from the stream's split
+            // counters (zero; the last slice of a column block resets its own)
+            cudaError_t e = sync.acquire(stream, static_cast<size_t>(a.n_cb), 0);
+            if (e != cudaSuccess) return e;
+            a.ws_count = sync.counters;
+            e = workspace_alloc(part, stream, &ws);
+            if (e != cudaSuccess) return e;
+            a.ws = static_cast<float *>(ws);
         }
-        a.ws = static_cast<float *>(ws);
     }
     const unsigned g = static_cast<unsigned>(grid);
     if (in == InType::F32) {
@@ -468,12 +494,12 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
         *name = p.b_kmajor ? "skinny<bf16,B:K>" : "skinny<bf16,B:N>";
     }
     cudaError_t e = cudaGetLastError();
-    for (void *owned : {ws, sync_owned}) {
-        if (owned == nullptr) continue;
-        const cudaError_t ef = workspace_free(owned, stream);
+    if (ws != nullptr) {
+        const cudaError_t ef = workspace_free(ws, stream);
         if (e == cudaSuccess) e = ef;
     }
-    return e;
+    const cudaError_t er = sync.release();
+    return e != cudaSuccess ? e : er;
 }
 
 }  // namespace gemm

@@ -15,11 +15,25 @@
 // kernels keeps the second one from starting as the first drains.  Flags
 // that pieces wait on are compared with a per-stream generation number that
 // grows with every call, so they are never cleared either.
+//
+// Streams are told apart by the stream's unique id (cudaStreamGetId), not
+// by the handle value: cudaStreamPerThread is one handle value for every
+// host thread but a different stream in each, and the legacy default stream
+// has two handle values (0 and cudaStreamLegacy).
+//
+// A call holds its stream's entry from SplitSync::acquire until the launch
+// is enqueued (SplitSync::release).  So, on one stream, launches are
+// enqueued in the order of the generation numbers they were given, and a
+// buffer that a stream outgrows is freed in stream order (cudaFreeAsync)
+// after every launch that was given it: any number of host threads may call
+// on one stream.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <memory>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -37,10 +51,7 @@ struct Pool {
 };
 Pool g_pools[kMaxDevices];
 
-cudaError_t device_pool(cudaMemPool_t *out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+cudaError_t pool_of(int dev, cudaMemPool_t *out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     Pool &p = g_pools[dev];
     std::call_once(p.once, [&p, dev] {
@@ -57,6 +68,20 @@ cudaError_t device_pool(cudaMemPool_t *out) {
     return p.err;
 }
 
+cudaError_t device_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return pool_of(dev, out);
+}
+
+cudaError_t pool_alloc(size_t bytes, cudaStream_t stream, void **ptr) {
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = device_pool(&pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
 }  // namespace
 
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr) {
@@ -66,107 +91,193 @@ cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr) {
     cudaError_t e = cudaStreamIsCapturing(stream, &capture);
     if (e != cudaSuccess) return e;
     if (capture != cudaStreamCaptureStatusNone) return cudaMallocAsync(ptr, bytes, stream);
-    cudaMemPool_t pool = nullptr;
-    if ((e = device_pool(&pool)) != cudaSuccess) return e;
-    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+    return pool_alloc(bytes, stream, ptr);
 }
 
 cudaError_t workspace_free(void *ptr, cudaStream_t stream) { return cudaFreeAsync(ptr, stream); }
 
 namespace {
 struct SyncBuf {
+    std::mutex m;  // held by a call from acquire until its launch is enqueued
+    int dev = 0;
     int *counters = nullptr;
     size_t n_counters = 0;
     unsigned *flags = nullptr;
     size_t n_flags = 0;
     unsigned generation = 0;
 };
-std::mutex g_sync_mutex;
-std::unordered_map<uint64_t, SyncBuf> g_sync;  // key: (device, stream)
-std::vector<void *> g_sync_retired;            // outgrown buffers, never freed
 
-uint64_t sync_key(int dev, cudaStream_t stream) {
-    return (static_cast<uint64_t>(dev) << 56) ^ reinterpret_cast<uintptr_t>(stream);
-}
+struct KeyHash {
+    size_t operator()(const std::pair<int, unsigned long long> &k) const {
+        return std::hash<unsigned long long>()(k.second * 0x9E3779B97F4A7C15ull ^
+                                               static_cast<unsigned long long>(k.first));
+    }
+};
 
-// A zeroed buffer of at least `want` words for one of the regions.  An
-// outgrown buffer is kept allocated: a launch enqueued by another host thread
-// may still hold its address.
+// Entries are created on a stream's first split call and never erased (an
+// entry is a few words; its buffers are freed by split_sync_release_device).
+std::mutex g_map_mutex;
+std::unordered_map<std::pair<int, unsigned long long>, std::unique_ptr<SyncBuf>, KeyHash> g_sync;
+
+// Buffer sizes grow in steps of 16 words (64 bytes): a stream holds about
+// what its largest split call needed (at most a few KiB).
+constexpr size_t kWords = 16;
+
+// A zeroed buffer of at least `want` words, allocated from the pool and
+// cleared on `stream`.  The outgrown buffer is freed on `stream`: every
+// launch that was given it was enqueued on `stream` before this call (the
+// entry is held from acquire to enqueue), so the free runs after them.
 template <typename T>
 cudaError_t ensure(T **ptr, size_t *have, size_t want, cudaStream_t stream) {
     if (*have >= want) return cudaSuccess;
-    size_t n = *have ? *have : 4096;
-    while (n < want) n *= 2;
+    const size_t n = (want + kWords - 1) / kWords * kWords;
     void *fresh = nullptr;
-    cudaError_t e = cudaMalloc(&fresh, n * sizeof(T));
+    cudaError_t e = pool_alloc(n * sizeof(T), stream, &fresh);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(fresh, 0, n * sizeof(T), stream);
     if (e != cudaSuccess) {
-        cudaFree(fresh);
+        cudaFreeAsync(fresh, stream);
         return e;
     }
-    if (*ptr != nullptr) g_sync_retired.push_back(*ptr);
+    T *old = *ptr;
     *ptr = static_cast<T *>(fresh);
     *have = n;
-    return cudaSuccess;
+    return old != nullptr ? cudaFreeAsync(old, stream) : cudaSuccess;
+}
+
+// Frees the buffers of every entry of `dev` after the device has finished
+// all work (the caller holds g_map_mutex).  Entries are locked first, so no
+// call can enqueue a launch with these counters meanwhile.
+cudaError_t release_device_locked(int dev) {
+    std::vector<std::unique_lock<std::mutex>> held;
+    for (auto &kv : g_sync)
+        if (kv.first.first == dev) held.emplace_back(kv.second->m);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    for (auto &kv : g_sync) {
+        SyncBuf &b = *kv.second;
+        if (b.dev != dev) continue;
+        for (void *p : {static_cast<void *>(b.counters), static_cast<void *>(b.flags)}) {
+            if (p == nullptr) continue;
+            const cudaError_t ef = cudaFreeAsync(p, cudaStreamLegacy);
+            if (e == cudaSuccess) e = ef;
+        }
+        b.counters = nullptr;
+        b.flags = nullptr;
+        b.n_counters = b.n_flags = 0;
+        b.generation = 0;
+    }
+    const cudaError_t es = cudaStreamSynchronize(cudaStreamLegacy);
+    return e != cudaSuccess ? e : es;
 }
 }  // namespace
 
-cudaError_t split_sync(cudaStream_t stream, size_t n_counters, size_t n_flags, int **counters,
-                       unsigned **flags, unsigned *generation, void **owned) {
-    *owned = nullptr;
+cudaError_t SplitSync::acquire(cudaStream_t stream, size_t n_counters, size_t n_flags) {
+    stream_ = stream;
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(stream, &capture);
     if (e != cudaSuccess) return e;
     if (capture != cudaStreamCaptureStatusNone) {
         // one zeroed block per captured launch: [counters][flags]
         const size_t c_bytes = (n_counters * sizeof(int) + 15) & ~static_cast<size_t>(15);
-        const size_t bytes = c_bytes + n_flags * sizeof(unsigned);
+        size_t bytes = c_bytes + n_flags * sizeof(unsigned);
+        if (bytes == 0) bytes = 16;
         void *blk = nullptr;
-        if ((e = workspace_alloc(bytes > 0 ? bytes : 16, stream, &blk)) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(blk, 0, bytes > 0 ? bytes : 16, stream)) != cudaSuccess) {
-            workspace_free(blk, stream);
-            return e;
-        }
-        *owned = blk;
-        if (counters) *counters = static_cast<int *>(blk);
-        if (flags) *flags = reinterpret_cast<unsigned *>(static_cast<char *>(blk) + c_bytes);
-        if (generation) *generation = 1;
+        if ((e = workspace_alloc(bytes, stream, &blk)) != cudaSuccess) return e;
+        owned_ = blk;
+        if ((e = cudaMemsetAsync(blk, 0, bytes, stream)) != cudaSuccess) return e;
+        counters = static_cast<int *>(blk);
+        flags = reinterpret_cast<unsigned *>(static_cast<char *>(blk) + c_bytes);
+        generation = 1;
         return cudaSuccess;
     }
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(g_sync_mutex);
-    SyncBuf &b = g_sync[sync_key(dev, stream)];
-    if ((e = ensure(&b.counters, &b.n_counters, n_counters, stream)) != cudaSuccess) return e;
-    if ((e = ensure(&b.flags, &b.n_flags, n_flags, stream)) != cudaSuccess) return e;
-    if (++b.generation == 0) {
-        // after 2^32 calls on one stream: start the flags over from zero
-        e = cudaMemsetAsync(b.flags, 0, b.n_flags * sizeof(unsigned), stream);
-        if (e != cudaSuccess) return e;
-        b.generation = 1;
+    unsigned long long id = 0;
+    if ((e = cudaStreamGetId(stream, &id)) != cudaSuccess) return e;
+    SyncBuf *b = nullptr;
+    {
+        std::lock_guard<std::mutex> map_lock(g_map_mutex);
+        std::unique_ptr<SyncBuf> &slot = g_sync[{dev, id}];
+        if (!slot) {
+            slot.reset(new SyncBuf);
+            slot->dev = dev;
+        }
+        b = slot.get();
     }
-    if (counters) *counters = b.counters;
-    if (flags) *flags = b.flags;
-    if (generation) *generation = b.generation;
+    lock_ = std::unique_lock<std::mutex>(b->m);
+    if ((e = ensure(&b->counters, &b->n_counters, n_counters, stream)) != cudaSuccess) return e;
+    if ((e = ensure(&b->flags, &b->n_flags, n_flags, stream)) != cudaSuccess) return e;
+    if (++b->generation == 0) {
+        // after 2^32 calls on one stream: start the flags over from zero
+        if (b->n_flags > 0) {
+            e = cudaMemsetAsync(b->flags, 0, b->n_flags * sizeof(unsigned), stream);
+            if (e != cudaSuccess) return e;
+        }
+        b->generation = 1;
+    }
+    counters = b->counters;
+    flags = b->flags;
+    generation = b->generation;
     return cudaSuccess;
 }
 
-cudaError_t split_sync_reset_device() {
+cudaError_t SplitSync::release() {
+    cudaError_t e = cudaSuccess;
+    if (owned_ != nullptr) {
+        e = workspace_free(owned_, stream_);
+        owned_ = nullptr;
+    }
+    if (lock_.owns_lock()) lock_.unlock();
+    return e;
+}
+
+SplitSync::~SplitSync() { release(); }
+
+cudaError_t split_sync_release_device() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(g_sync_mutex);
-    for (auto &kv : g_sync) {
-        if (static_cast<int>(kv.first >> 56) != dev) continue;
-        SyncBuf &b = kv.second;
-        if (b.counters && (e = cudaMemset(b.counters, 0, b.n_counters * sizeof(int))) != cudaSuccess)
-            return e;
-        if (b.flags && (e = cudaMemset(b.flags, 0, b.n_flags * sizeof(unsigned))) != cudaSuccess)
-            return e;
-        b.generation = 0;
+    std::lock_guard<std::mutex> map_lock(g_map_mutex);
+    return release_device_locked(dev);
+}
+
+cudaError_t memory_info(MemoryInfo *out) {
+    *out = MemoryInfo{};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> map_lock(g_map_mutex);
+        for (auto &kv : g_sync) {
+            if (kv.first.first != dev) continue;
+            std::lock_guard<std::mutex> entry_lock(kv.second->m);
+            const SyncBuf &b = *kv.second;
+            const uint64_t bytes = b.n_counters * sizeof(int) + b.n_flags * sizeof(unsigned);
+            if (bytes == 0) continue;
+            ++out->split_streams;
+            out->split_bytes += bytes;
+        }
     }
-    return cudaDeviceSynchronize();
+    cudaMemPool_t pool = nullptr;
+    if ((e = pool_of(dev, &pool)) != cudaSuccess) return e;
+    unsigned long long used = 0, reserved = 0;
+    if ((e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &used)) != cudaSuccess)
+        return e;
+    if ((e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &reserved)) !=
+        cudaSuccess)
+        return e;
+    out->pool_used_bytes = used;
+    out->pool_reserved_bytes = reserved;
+    return cudaSuccess;
+}
+
+cudaError_t release_memory() {
+    cudaError_t e = split_sync_release_device();
+    if (e != cudaSuccess) return e;
+    cudaMemPool_t pool = nullptr;
+    if ((e = device_pool(&pool)) != cudaSuccess) return e;
+    return cudaMemPoolTrimTo(pool, 0);
 }
 
 }  // namespace gemm

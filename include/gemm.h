@@ -29,17 +29,22 @@
  *   keep every SM busy).  Such a kernel takes a temporary workspace for the
  *   partial sums (a few tens of MiB at most) from a memory pool the library
  *   owns, one per device, allocated and freed in stream order on `stream`.
- *   The pool keeps up to 256 MiB of freed memory for later calls.  The split
- *   pieces count themselves in small counters that the library keeps per
- *   (device, stream) and that every kernel returns to zero, so no call
- *   clears them.  These take 32 KiB per stream at first (more only for
- *   problems with more split tiles) and are kept until the process ends.
+ *   The pool keeps up to 256 MiB of freed memory for later calls.
+ *   Split counters: the split pieces count themselves in small counters that
+ *   the library keeps per (device, stream) -- streams told apart by their
+ *   unique id, so cudaStreamPerThread is a different stream in each host
+ *   thread -- and that every kernel returns to zero, so no call clears them.
+ *   They take what the largest split call on the stream needed (64 bytes
+ *   to a few KiB) and come from the same pool.  A stream's counters that
+ *   a larger problem outgrows are freed in stream order.  What a device
+ *   holds is reported by gemm_memory_info(); gemm_release_memory() frees it.
  *   Graph capture: while `stream` is being captured, each call takes fresh
  *   counters and workspace as graph memory.  The graph may therefore be
  *   replayed on any stream, beside other calls.
- *   Threads: calls may come from several host threads.  Calls on one stream
- *   must not be made from two threads at once: like the stream's own order,
- *   the counters assume that calls on a stream run one after another.
+ *   Threads: any number of host threads may call at once, on one stream or
+ *   on several.  A call holds its stream's counters from the moment it takes
+ *   them until its kernel is enqueued, so calls on one stream are enqueued
+ *   one after another.
  * Asynchrony: the work is enqueued on `stream` (0 = the legacy default
  *   stream) and the call returns without waiting for it.  The caller keeps
  *   the buffers alive until the stream has passed the call.
@@ -163,31 +168,35 @@ gemm_status_t gemm_f16_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
 
 /*
  * gemm_f32_noalloc -- gemm_f32 for callers that cannot allocate device
- * memory.  The GEMM pages have no counterpart to this entry point; it exists
- * for code that runs under a device-memory budget fixed in advance, or on
- * paths where calling the CUDA allocator is not allowed (for example inside
- * an allocator's own callbacks, or where an allocation could block).
+ * memory.  The GEMM pages have no counterpart to this entry point.  It is
+ * for code that must not call the CUDA allocator: code running under a
+ * device-memory budget fixed in advance, code inside an allocator's own
+ * callbacks, or code on a path where an allocation could block or fail.
  *
- * Arguments, results and accuracy are those of gemm_f32, and it runs the
- * same kernel with the same work split.  The only difference: when the
- * kernel splits the K range of its last tiles, the partial sums go to a
- * fixed 32 MiB array compiled into the library (a file-scope __device__
+ * Arguments, results and accuracy are those of gemm_f32, and it picks the
+ * same kernel with the same work split (the small-M kernel for M <= 8, the
+ * cluster kernel for small problems, the CUDA-core kernel's tile
+ * configurations otherwise).  The only difference: when that kernel splits
+ * the K range of some tiles, the split pieces' counters and partial sums go
+ * to a fixed 32 MiB array compiled into the library (a file-scope __device__
  * array that every device holding the library keeps until the process
- * exits) instead of pool memory, so the call allocates nothing: no
- * cudaMalloc, no cudaFree, no pool.
+ * exits) instead of pool memory and the stream's counters.  So the call
+ * allocates nothing: no cudaMalloc, no cudaFree, no pool.
  *
  * Limits and rules:
- *   - A problem whose split needs more than 32 MiB of partial sums is
- *     refused with GEMM_ERR_INVALID_VALUE before anything is enqueued
- *     (gemm_f32 handles it).  Problems that split no tile need no scratch.
- *   - The first call on each device looks up that device's address of the
- *     array (cudaGetSymbolAddress); make that first call before any stream
- *     capture on that device.
- *   - All calls on a device share the one array, and it keeps what the last
- *     call left in it; each call clears the counters it needs.  Calls whose
- *     work overlaps on the GPU (different streams, no ordering between them)
- *     race on the array and give wrong results: order them on one stream or
- *     with events.
+ *   - The first 16 KiB of the array hold the counters, the rest (32 MiB -
+ *     16 KiB) the partial sums.  A problem whose split needs more is refused
+ *     with GEMM_ERR_INVALID_VALUE before anything is enqueued (gemm_f32
+ *     handles it).  Problems that split no tile need no scratch.
+ *   - The first call on each device sets up the array: it looks up that
+ *     device's address of it (cudaGetSymbolAddress), zeroes the counters on
+ *     `stream` and waits for that.  Make that first call before any stream
+ *     capture on that device (under capture it returns GEMM_ERR_INTERNAL).
+ *   - Every kernel leaves the counters it used at zero, so later calls clear
+ *     nothing.  All calls on a device share the one array, and it keeps what
+ *     the last call left in it.  Calls whose work overlaps on the GPU
+ *     (different streams, no ordering between them) race on the array and
+ *     give wrong results: order them on one stream or with events.
  */
 gemm_status_t gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                const float *A, int64_t lda, gemm_order_t order_a,
@@ -244,12 +253,43 @@ const char *gemm_status_string(gemm_status_t status);
  * the current device's status word.  Returns GEMM_OK, or GEMM_ERR_TIMEOUT if
  * a tensor-core launch on this device gave up a bounded wait since the last
  * read (its D is then incomplete), or GEMM_ERR_INTERNAL if the read itself
- * failed.  After a timeout it also returns the device's split counters (the
- * counts of finished K pieces that each stream keeps between calls, and that
- * a kernel which gave up may have left mid-count) to zero, synchronising the
- * device; read it after a timeout before the next call on this device.
+ * failed.  After a timeout it also synchronises the device and frees every
+ * stream's split counters (the counts of finished K pieces that each stream
+ * keeps between calls, and that a kernel which gave up may have left
+ * mid-count); the next split call on a stream starts from zeroed ones.  Read
+ * it after a timeout before the next call on this device.
  */
 gemm_status_t gemm_last_device_status(cudaStream_t stream);
+
+/*
+ * What the library holds on the current device between calls (the split
+ * counters of each stream and the workspace pool; see "Split counters" and
+ * "Workspace" above).  Nothing in the pages corresponds to this: it is the
+ * accounting of this library's own memory.
+ *   split_streams        streams of this device that hold split counters
+ *   split_bytes          bytes of those counters
+ *   pool_used_bytes      pool memory in use: the split counters, plus the
+ *                        workspace of calls the GPU has not finished yet
+ *   pool_reserved_bytes  pool memory held from the driver (in use or kept
+ *                        for reuse, at most 256 MiB beyond what is in use)
+ * Returns GEMM_ERR_INVALID_VALUE for a NULL info, GEMM_ERR_INTERNAL if a
+ * CUDA query failed.
+ */
+typedef struct {
+    uint64_t split_streams;
+    uint64_t split_bytes;
+    uint64_t pool_used_bytes;
+    uint64_t pool_reserved_bytes;
+} gemm_memory_info_t;
+gemm_status_t gemm_memory_info(gemm_memory_info_t *info);
+
+/*
+ * gemm_release_memory -- synchronises the current device, frees the split
+ * counters of every stream on it and returns the pool's free memory to the
+ * driver.  Later calls take what they need again.  Call it when no other
+ * host thread is calling the library on this device.
+ */
+gemm_status_t gemm_release_memory(void);
 
 /*
  * gemm_last_kernel -- name of the kernel the calling host thread's most

@@ -8,7 +8,9 @@ zero, so no call clears them (a captured call takes fresh zeroed counters
 instead).  These tests check that calls of every variant -- back to back in
 any order, on two streams at once, after a kernel gave up a bounded wait, and
 replayed from a captured graph beside eager calls -- give the same bits as a
-first call that is checked against the oracle."""
+first call that is checked against the oracle.  Calls may come from any
+number of host threads, on one stream or on several (cudaStreamPerThread
+included); counters a stream outgrows are freed in stream order."""
 import numpy as np
 import pytest
 import torch
@@ -175,3 +177,120 @@ def test_host_threads_on_their_own_streams(cases):
     for t, out in got.items():
         for i, D in out:
             assert torch.equal(D, first[i]), (t, cases[i].w.name)
+
+
+def test_host_threads_on_one_stream(cases):
+    """Two host threads call every split variant on the SAME stream at once:
+    a call holds the stream's counters until its kernel is enqueued, so the
+    launches of the stream are enqueued one after another and every result
+    is bit-identical to the oracle-checked first call."""
+    import threading
+    first = _first_results(cases)
+    for c, D in zip(cases, first):
+        c.check_against_oracle(D)
+    shared = torch.cuda.Stream()
+    shared.wait_stream(torch.cuda.current_stream())
+    got, errors = {}, []
+    barrier = threading.Barrier(2)
+
+    def worker(t):
+        try:
+            out = []
+            barrier.wait()
+            with torch.cuda.stream(shared):
+                for rep in range(4):
+                    for i in range(len(cases)):
+                        j = (i + 3 * t + rep) % len(cases)
+                        out.append((j, cases[j].launch(shared)))
+            got[t] = out
+        except Exception as e:  # surfaced below, in the test's thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    assert sorted(got) == [0, 1]
+    for t, out in got.items():
+        for i, D in out:
+            assert torch.equal(D, first[i]), (t, cases[i].w.name)
+
+
+def test_per_thread_default_stream_in_two_threads(cases):
+    """cudaStreamPerThread is one handle value but a different stream in each
+    host thread; the library tells the streams apart by their unique id, so
+    two threads calling the split variants on it at once keep separate
+    counters and get the first call's bits."""
+    import threading
+    per_thread = 2  # cudaStreamPerThread
+    first = _first_results(cases)
+    got, errors = {}, []
+    barrier = threading.Barrier(2)
+
+    def worker(t):
+        try:
+            out = []
+            barrier.wait()
+            for rep in range(4):
+                for i in range(len(cases)):
+                    j = (i + t + rep) % len(cases)
+                    out.append((j, cases[j].launch(per_thread)))
+            torch.cuda.synchronize()
+            got[t] = out
+        except Exception as e:  # surfaced below, in the test's thread
+            errors.append(repr(e))
+
+    torch.cuda.synchronize()
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+    for t, out in got.items():
+        for i, D in out:
+            assert torch.equal(D, first[i]), (t, cases[i].w.name)
+
+
+def test_outgrown_counters_are_freed():
+    """Ten calls on one stream, each splitting more tiles than the last, grow
+    the stream's counters ten times; each outgrown buffer is freed in stream
+    order, so afterwards the stream holds one buffer (the last size) and the
+    pool has nothing else in use.  gemm_release_memory frees even that, and
+    the next call starts from fresh counters.  Every result is checked
+    against the oracle."""
+    lib.gemm_release_memory()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    sizes = []
+    # 128 x 256 tiles, one column of them: t tiles split K (t < 76 on GB300),
+    # each with 4 counters and 4 flags
+    for t in (1, 5, 9, 13, 17, 21, 25, 29, 33, 37, 41):
+        w = Workload(f"grow_{t}", 128 * t, 256, 1024, 1.0, 0.0, "bf16", ROW, COL, ROW)
+        c = Case(w, "gemm_bf16_tc<splitk>", seed=t)
+        D = c.launch(s)
+        s.synchronize()
+        c.check_against_oracle(D)
+        info = lib.gemm_memory_info()
+        assert info["split_streams"] == 1, info
+        sizes.append(info["split_bytes"])
+        assert info["pool_used_bytes"] == info["split_bytes"], info
+    assert all(b > a for a, b in zip(sizes, sizes[1:])), sizes  # ten growths
+    # counters + flags of the last call only, each 164 words rounded up to 16
+    assert sizes[-1] == 2 * 176 * 4, sizes
+    assert lib.gemm_release_memory() == lib.GEMM_OK
+    info = lib.gemm_memory_info()
+    assert info["split_streams"] == 0 and info["split_bytes"] == 0, info
+    assert info["pool_used_bytes"] == 0 and info["pool_reserved_bytes"] == 0, info
+    w = Workload("after_release", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW)
+    c = Case(w, "gemm_bf16_tc<splitk>", seed=99)
+    D = c.launch(s)
+    s.synchronize()
+    c.check_against_oracle(D)
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
