@@ -34,7 +34,10 @@ GEMM_ERR_LAUNCH = 3
 GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_INTERNAL = 5
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
+# DENSE_GEMM_08_GB300_LIB names another build of the same library (for
+# example a variant from _build.build_variant); by default the in-tree build.
+LIB_PATH = os.environ.get("DENSE_GEMM_08_GB300_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libdense_gemm_08_gb300.so")
 EXPORTED = ("gemm_f32", "gemm_bf16_f32acc", "gemm_f16_f32acc", "gemm_bf16_f32acc_ex",
             "gemm_f32_noalloc", "gemm_status_string", "gemm_last_device_status",
             "gemm_last_kernel", "gemm_memory_info", "gemm_release_memory",

@@ -83,5 +83,31 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+def build_variant(tag: str, defines: dict, units=("gemm_tc.cu",), verbose: bool = False) -> str:
+    """A second build of the library with preprocessor `defines` applied to
+    `units` (the other translation units are the default build's objects),
+    in _build/<tag>/; returns its path.  For measurements that compare a
+    compile-time choice (e.g. the ring depth) in otherwise the same library."""
+    build(verbose=verbose)
+    out_dir = os.path.join(BUILD_DIR, tag)
+    os.makedirs(out_dir, exist_ok=True)
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    nvcc = _nvcc()
+    objs = []
+    for src in SOURCES:
+        if src not in units:
+            objs.append(os.path.join(BUILD_DIR, src.replace(".cu", ".o")))
+            continue
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        objs.append(obj)
+        with open(os.path.join(out_dir, "ptxas_" + src.replace(".cu", ".log")), "w") as log:
+            subprocess.run([nvcc, *NVCC_FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj],
+                           stdout=log, stderr=subprocess.STDOUT, check=True)
+    lib = os.path.join(out_dir, LIB_NAME)
+    subprocess.run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", lib,
+                    *objs], check=True)
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))

@@ -57,6 +57,15 @@ constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
 constexpr int NUM_THREADS = 192;          // 6 warps
 constexpr int kGroupM = 8;                // grouped raster width (tile rows)
 
+// Depth of the CTA pair's operand ring (stages of 32 KiB per CTA).  Six is
+// the most that fit beside the epilogue boxes; a build may set fewer
+// (-DGEMM_TC_PAIR_STAGES=S, 2 <= S <= 6) to measure throughput against depth.
+#ifndef GEMM_TC_PAIR_STAGES
+#define GEMM_TC_PAIR_STAGES 6
+#endif
+static_assert(GEMM_TC_PAIR_STAGES >= 2 && GEMM_TC_PAIR_STAGES <= 6,
+              "the pair ring holds 2 to 6 stages");
+
 template <int CG>
 struct Cfg {
     static constexpr int TILE_M = BM * CG;  // tile rows covered by the CTA group
@@ -64,11 +73,12 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr int STAGES = CG == 1 ? 4 : GEMM_TC_PAIR_STAGES;
     // epilogue staging: per epilogue warp two 32 x 32 FP32 boxes (4 KiB each)
     static constexpr int STAGING_BYTES = 4 * 2 * 32 * 32 * 4;
     // ring + staging + barriers + slack for aligning the ring to 1024 bytes
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
 __device__ int g_tc_status;  // 0 = fine, 1 = a bounded wait ran out

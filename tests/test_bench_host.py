@@ -127,3 +127,66 @@ def test_rotation_copies_exceed_twice_l2():
     assert bench.rotation_copies(192 * 2**20, l2) == 2
     assert bench.rotation_copies(512 * 2**20, l2) == 1
     assert bench.rotation_copies(2 * l2, l2) == 1
+
+
+def test_region_clocks_take_the_samples_inside_the_timed_region():
+    nvml = [{"t": 10.000, "sm": 1500.0, "max": 2070.0, "power": 200.0, "reasons": []},
+            {"t": 10.004, "sm": 2070.0, "max": 2070.0, "power": 900.0, "reasons": []},
+            {"t": 10.005, "sm": 2055.0, "max": 2070.0, "power": 1100.0,
+             "reasons": ["sw_power_cap"]},
+            {"t": 10.006, "sm": 2040.0, "max": 2070.0, "power": 1200.0, "reasons": []},
+            {"t": 10.050, "sm": 1200.0, "max": 2070.0, "power": 150.0,
+             "reasons": ["hw_slowdown"]}]
+    smi = [{"t": 9.95, "sm": 1400.0, "max": 2070.0, "power": 180.0, "reasons": []}]
+    c = bench.region_clocks(nvml, smi, 10.003, 10.010)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2055.0 and c["sm_mhz_min"] == 2040.0
+    assert c["reasons"] == ["sw_power_cap"]  # the slowdown came after the region
+    assert c["power_w_max"] == 1200.0 and c["sm_max_mhz"] == 2070.0
+    assert c["source"].startswith("NVML")
+    # no NVML samples: the run-wide nvidia-smi summary stands in
+    c = bench.region_clocks([], smi, 10.003, 10.010)
+    assert c["samples"] == 0 and c["sm_mhz"] == 1400.0
+
+
+def test_reference_arm_prints_the_same_config_as_ours():
+    w = WORKLOADS["bf16_8192"]
+    ours = bench.workload_config(w, queue="gpu", l2="x")
+    ref = bench.workload_config(w, queue="cpu")
+    shared = set(ours) & set(ref)
+    assert {"workload", "M", "N", "K", "alpha", "beta", "in_dtype", "acc_dtype", "out_dtype",
+            "order_a", "order_b", "order_cd", "inputs"} <= shared
+    assert all(ours[k] == ref[k] for k in shared if k != "queue")
+    assert ours["order_b"] == "col" and ours["in_dtype"] == "bf16"
+
+
+def test_pipeline_depth_fits_recover_their_models():
+    # exact data of each model: the fit returns its parameters
+    S = [2, 3, 4, 5, 6]
+    P, kappa, rms = bench.fit_saturating(S, [2000 * s / (s + 1.5) for s in S])
+    assert P == pytest.approx(2000, rel=1e-4) and kappa == pytest.approx(1.5, rel=1e-4)
+    assert rms < 1e-3
+    P, b, rms = bench.fit_littles_law(S, [min(1800.0, 400.0 * s) for s in S])
+    assert P == pytest.approx(1800.0) and b == pytest.approx(400.0) and rms < 1e-9
+
+
+def test_committed_pipeline_depth_sweep_refits_to_its_stated_fits():
+    import re
+    path = os.path.join(bench.ROOT, "profiles", "gemm_bf16_tc_pipeline_depth_sweep.md")
+    text = open(path).read()
+    stages = eval(re.search(r"^stages: (\[.*\])$", text, re.M).group(1))
+    for wl in ("bf16_8192", "bf16_mlp"):
+        med = eval(re.search(rf"^{wl}_tflops_median: (\[.*\])$", text, re.M).group(1))
+        sat = dict(re.findall(r"(\w+)=([0-9.]+)",
+                              re.search(rf"^fit_{wl}_saturating: (.*)$", text, re.M).group(1)))
+        lit = dict(re.findall(r"(\w+)=([0-9.]+)",
+                              re.search(rf"^fit_{wl}_littles_law: (.*)$", text, re.M).group(1)))
+        P, kappa, rms = bench.fit_saturating(stages, med)
+        assert P == pytest.approx(float(sat["P"]), rel=1e-3)
+        assert kappa == pytest.approx(float(sat["kappa"]), rel=1e-3)
+        assert rms == pytest.approx(float(sat["rms"]), rel=1e-3)
+        P, b, rms = bench.fit_littles_law(stages, med)
+        assert P == pytest.approx(float(lit["P"]), rel=1e-4)
+        assert b == pytest.approx(float(lit["b"]), rel=1e-4)
+        assert rms == pytest.approx(float(lit["rms"]), rel=1e-3)
+        # the piecewise bound fits the measurements better than the smooth curve
+        assert rms < float(sat["rms"])
