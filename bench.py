@@ -797,18 +797,21 @@ def fit_littles_law(S, T):
 
 def bench_sweep_stages(args):
     """--sweep-stages S1,S2,...: builds the library once per CTA-pair ring
-    depth (-DGEMM_TC_PAIR_STAGES=S, only the tensor-core unit recompiled) and
-    times BF16 8192^3 and the MLP shape with each, in a fresh process per
-    depth, over --sweep-reps rounds in rotated order; prints the median
-    TFLOPS per depth and the two fits as one JSON line."""
+    depth S (only the tensor-core unit recompiled: the direct-epilogue ring,
+    which BF16 8192^3 runs, gets S stages, -DGEMM_TC_DIRECT_STAGES=S; the
+    staged ring, which the MLP shape's beta = 1 needs, min(S, 6)) and times
+    BF16 8192^3 and the MLP shape with each, in a fresh process per depth,
+    over --sweep-reps rounds in rotated order; prints the median TFLOPS per
+    depth and the two fits as one JSON line."""
     from concurrent.futures import ThreadPoolExecutor
     from dense_gemm_08_gb300 import _build
 
     stages = [int(x) for x in args.sweep_stages.split(",")]
     _build.build()
     with ThreadPoolExecutor(len(stages)) as ex:
-        paths = list(ex.map(lambda S: _build.build_variant(f"stages{S}",
-                                                           {"GEMM_TC_PAIR_STAGES": S}), stages))
+        paths = list(ex.map(lambda S: _build.build_variant(
+            f"stages{S}", {"GEMM_TC_DIRECT_STAGES": S, "GEMM_TC_PAIR_STAGES": min(S, 6)}),
+            stages))
     libs = dict(zip(stages, paths))
     runs = {"bf16_8192": {S: [] for S in stages}, "bf16_mlp": {S: [] for S in stages}}
     clocks = {S: [] for S in stages}
@@ -920,7 +923,7 @@ def main(argv=None):
                     help="workloads timed after the headline, each in its own region "
                          "(comma list, or 'none')")
     ap.add_argument("--sweep-stages", default=None,
-                    help="comma list of CTA-pair ring depths to build and time (2..6)")
+                    help="comma list of CTA-pair ring depths to build and time (2..7)")
     ap.add_argument("--sweep-reps", type=int, default=2)
     ap.add_argument("--probe", action="store_true",
                     help="time the library's peak probes instead of a GEMM workload")

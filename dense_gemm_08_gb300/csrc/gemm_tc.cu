@@ -16,7 +16,9 @@
 //     tcgen05.mma (one lane), warps 2-5 run the epilogue.
 //   * Persistent grid, static round-robin over output tiles in grouped order
 //     along M so that tiles running together share A and B panels in L2
-//     ("GEMM on NVIDIA GPUs", section 5 / grouped schedulers).
+//     ("GEMM on NVIDIA GPUs", section 5 / grouped schedulers); every other
+//     round walks K backwards, so a round starts on the K blocks the one
+//     before it read last (still in L2).
 //   * Two TMEM accumulators (2 x 256 columns): the epilogue of tile i runs
 //     while the MMA warp accumulates tile i + 1.
 //   * Epilogue: tcgen05.ld TMEM -> registers, D = alpha * acc + beta * C
@@ -55,27 +57,41 @@ constexpr int BN = 256;  // tile width = MMA N
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
 constexpr int NUM_THREADS = 192;          // 6 warps
-constexpr int kGroupM = 8;                // grouped raster width (tile rows)
+constexpr int kGroupM = 16;               // grouped raster width (tile rows)
 
-// Depth of the CTA pair's operand ring (stages of 32 KiB per CTA).  Six is
-// the most that fit beside the epilogue boxes; a build may set fewer
-// (-DGEMM_TC_PAIR_STAGES=S, 2 <= S <= 6) to measure throughput against depth.
+// Depth of the CTA pair's operand ring (stages of 32 KiB per CTA).  With the
+// epilogue's staging boxes six stages fit; without them (the direct
+// epilogue, below) seven.  A build may set fewer (-DGEMM_TC_PAIR_STAGES=S,
+// 2 <= S <= 6; -DGEMM_TC_DIRECT_STAGES=S, 2 <= S <= 7) to measure
+// throughput against depth.
 #ifndef GEMM_TC_PAIR_STAGES
 #define GEMM_TC_PAIR_STAGES 6
 #endif
+#ifndef GEMM_TC_DIRECT_STAGES
+#define GEMM_TC_DIRECT_STAGES 7
+#endif
 static_assert(GEMM_TC_PAIR_STAGES >= 2 && GEMM_TC_PAIR_STAGES <= 6,
-              "the pair ring holds 2 to 6 stages");
+              "the staged pair ring holds 2 to 6 stages");
+static_assert(GEMM_TC_DIRECT_STAGES >= 2 && GEMM_TC_DIRECT_STAGES <= 7,
+              "the direct pair ring holds 2 to 7 stages");
 
-template <int CG>
+// DIRECT (CTA pairs only): the epilogue moves each accumulator row from
+// registers straight to D with 32-byte stores, and a split tile's pieces
+// travel the same way, so the kernel needs no staging boxes and the ring
+// takes their shared memory.  For beta = 0 and D rows that start on
+// 32 bytes.
+template <int CG, bool DIRECT = false>
 struct Cfg {
+    static_assert(!DIRECT || CG == 2, "the direct epilogue is built for CTA pairs");
     static constexpr int TILE_M = BM * CG;  // tile rows covered by the CTA group
     static constexpr int B_ROWS = BN / CG;  // B columns (N) held by each CTA
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = CG == 1 ? 4 : GEMM_TC_PAIR_STAGES;
+    static constexpr int STAGES =
+        CG == 1 ? 4 : (DIRECT ? GEMM_TC_DIRECT_STAGES : GEMM_TC_PAIR_STAGES);
     // epilogue staging: per epilogue warp two 32 x 32 FP32 boxes (4 KiB each)
-    static constexpr int STAGING_BYTES = 4 * 2 * 32 * 32 * 4;
+    static constexpr int STAGING_BYTES = DIRECT ? 0 : 4 * 2 * 32 * 32 * 4;
     // ring + staging + barriers + slack for aligning the ring to 1024 bytes
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
@@ -516,14 +532,89 @@ __device__ __forceinline__ void box_store_rows_bf16(const uint8_t *box, const Tc
     }
 }
 
+// 32 bytes (eight 32-bit words) to global memory in one store.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
+// 32 bytes from global memory through L2 only (data other CTAs wrote).
+__device__ __forceinline__ void ld_global_cg_v8(const float *p, float (&v)[8]) {
+    asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "l"(p)
+                 : "memory");
+}
+
+// Direct epilogue: bias, activation and the store of one lane's 32 values
+// o[j] = D(row, c0 + j), from registers straight to D (32-byte stores when
+// the 32 columns are inside the matrix, guarded scalar stores at its edge).
+__device__ __forceinline__ void store_row_direct(float (&o)[32], const TcArgs &a, int64_t row,
+                                                 int64_t c0) {
+    if (a.bias != nullptr) {
+        if (a.bias_per_row) {
+            const float bv = row < a.M ? a.bias[row] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] += bv;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] += c0 + j < a.N ? a.bias[c0 + j] : 0.f;
+        }
+    }
+    if (a.act != kActNone) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = apply_activation(o[j], a.act);
+    }
+    if (row >= a.M) return;
+    const bool whole = c0 + 32 <= a.N;
+    if (a.d_bf16) {
+        uint16_t *d = reinterpret_cast<uint16_t *>(a.D) + row * a.ldd + c0;
+        if (whole) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                st_global_v8(d + q * 16, pack_bf16x2(o[q * 16 + 0], o[q * 16 + 1]),
+                             pack_bf16x2(o[q * 16 + 2], o[q * 16 + 3]),
+                             pack_bf16x2(o[q * 16 + 4], o[q * 16 + 5]),
+                             pack_bf16x2(o[q * 16 + 6], o[q * 16 + 7]),
+                             pack_bf16x2(o[q * 16 + 8], o[q * 16 + 9]),
+                             pack_bf16x2(o[q * 16 + 10], o[q * 16 + 11]),
+                             pack_bf16x2(o[q * 16 + 12], o[q * 16 + 13]),
+                             pack_bf16x2(o[q * 16 + 14], o[q * 16 + 15]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < a.N) d[j] = to_bf16_bits(o[j]);
+        }
+    } else {
+        float *d = a.D + row * a.ldd + c0;
+        if (whole) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_global_v8(d + q * 8, __float_as_uint(o[q * 8 + 0]),
+                             __float_as_uint(o[q * 8 + 1]), __float_as_uint(o[q * 8 + 2]),
+                             __float_as_uint(o[q * 8 + 3]), __float_as_uint(o[q * 8 + 4]),
+                             __float_as_uint(o[q * 8 + 5]), __float_as_uint(o[q * 8 + 6]),
+                             __float_as_uint(o[q * 8 + 7]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < a.N) d[j] = o[j];
+        }
+    }
+}
+
 // ------------------------------------------------------------------- kernel
-template <int CG>
+template <int CG, bool DIRECT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_d, const TcArgs args) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, DIRECT>;
     extern __shared__ uint8_t smem_raw[];
     // the ring must be 1024-byte aligned for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -592,13 +683,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t w = group_id; w < n_items && ok; w += num_groups) {
+            int64_t li = 0;
+            for (int64_t w = group_id; w < n_items && ok; w += num_groups, ++li) {
                 const WorkItem it = work_item<CG>(w, args);
                 int64_t tm, tn;
                 tile_coords(it.t, args, tm, tn);
                 const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
                 const int32_t n0 = static_cast<int32_t>(tn * BN + rank * C::B_ROWS);
-                for (int64_t kb = it.kb_begin; kb < it.kb_end; ++kb) {
+                // Serpentine K order: every other work item walks its K blocks
+                // backwards, so the blocks a round of tiles reads last are the
+                // ones the next round (the same tile rows, under the grouped
+                // raster) reads first, while they are still in L2.  The MMA
+                // side takes the stages as they come (the sum's order changes,
+                // not its terms).
+                const bool reverse = (li & 1) != 0;
+                for (int64_t i = 0; i < it.kb_end - it.kb_begin; ++i) {
+                    const int64_t kb = reverse ? it.kb_end - 1 - i : it.kb_begin + i;
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                       args.timeout_ns)) {
                         raise_abort(abort_flag);
@@ -742,6 +842,120 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!wait_bounded(smem_addr(drain), 0, &never, args.timeout_ns))
                 raise_abort(abort_flag);
             aborted = !ok;
+        }
+        __syncwarp();
+    } else if constexpr (DIRECT) {
+        // ------------------------------------------ epilogue warps 2-5, direct
+        // Per tile, the warp drains its 32 accumulator rows (TMEM lanes) in
+        // 32-column chunks: tcgen05.ld -> alpha * acc (bias, activation) in
+        // registers -> each lane stores its row's 32 values to D with
+        // 32-byte stores.  beta = 0: C is not read.  A split tile's pieces
+        // publish their raw sums the same way (one 32 x 32 block of rows per
+        // warp and chunk) and the last piece adds them, in K order, straight
+        // from global memory.
+        const int quarter = warp % 4;  // TMEM lanes this warp may access
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        int64_t li = 0;
+        for (int64_t w = group_id; w < n_items; w += num_groups, ++li) {
+            const WorkItem it = work_item<CG>(w, args);
+            const int64_t t = it.t;
+            const int buf = static_cast<int>(li & 1);
+            const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
+            // lane 0 waits, the warp follows its verdict (keeps the warp converged)
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_addr(&tfull[buf]), acc_phase, abort_flag, args.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_abort(abort_flag);
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            int64_t tm, tn;
+            tile_coords(t, args, tm, tn);
+            const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
+            const int64_t row = row0 + lane;                                 // this lane's row
+            const int64_t col0 = tn * BN;
+            int n_chunks = 0;  // chunks holding part of D (warp-uniform)
+            if (row0 < args.M) {
+                const int64_t rest = args.N - col0;
+                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+            }
+            const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
+            auto release_acc = [&]() {
+                // accumulator rows read: hand the buffer back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_addr(&tempty[buf]), 0));
+            };
+            if (it.nsp > 1 && n_chunks > 0) {
+                // ---- a split tail tile: publish this piece's raw sums, count
+                // the piece; the last piece to be counted adds all pieces in
+                // K order and writes D (no piece waits for another)
+                auto piece_row = [&](int piece, int chunk) -> float * {
+                    const int64_t slot = ((t - args.tail_first) * it.nsp + piece) * 2 + rank;
+                    return args.ws + ((slot * 4 + quarter) * 8 + chunk) * 1024 + lane * 32;
+                };
+                int *const counter = args.ws_count + ((t - args.tail_first) * 2 + rank) * 4 + quarter;
+#pragma unroll 1
+                for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                    uint32_t v[32];
+                    __syncwarp();  // tcgen05.ld is warp-collective: converge first
+                    tmem_load_32cols(t_acc + chunk * 32, v);
+                    float *dst = piece_row(it.sp, chunk);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_global_v8(dst + q * 8, v[q * 8 + 0], v[q * 8 + 1], v[q * 8 + 2],
+                                     v[q * 8 + 3], v[q * 8 + 4], v[q * 8 + 5], v[q * 8 + 6],
+                                     v[q * 8 + 7]);
+                }
+                release_acc();
+                __threadfence();  // each lane's sums are visible device-wide before the count
+                __syncwarp();
+                int reduce = 0;
+                if (lane == 0) {
+                    const int before = atomicAdd(counter, 1);
+                    reduce = before == it.nsp - 1;
+                    if (reduce) *counter = 0;  // all pieces counted: ready for the next call
+                }
+                __syncwarp();
+                reduce = __shfl_sync(0xffffffffu, reduce, 0);
+                if (!reduce) continue;
+                __threadfence();  // the other pieces' sums (read through L2) after the count
+#pragma unroll 1
+                for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                    float o[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                    for (int s2 = 0; s2 < it.nsp; ++s2) {  // K order
+                        const float *src = piece_row(s2, chunk);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float pv[8];
+                            ld_global_cg_v8(src + q * 8, pv);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) o[q * 8 + j] += pv[j];
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
+                    store_row_direct(o, args, row, col0 + chunk * 32);
+                }
+                continue;
+            }
+#pragma unroll 1
+            for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                uint32_t v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective: converge first
+                tmem_load_32cols(t_acc + chunk * 32, v);
+                if (chunk == n_chunks - 1) release_acc();
+                float o[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                store_row_direct(o, args, row, col0 + chunk * 32);
+            }
+            if (n_chunks == 0) release_acc();
         }
         __syncwarp();
     } else {
@@ -1236,7 +1450,8 @@ struct DeviceInfo {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     int sms = 1;
-    int pairs = 0;  // CTA pairs that can be resident at once (0: pair variant not used)
+    int pairs = 0;         // CTA pairs that can be resident at once (0: pair variant not used)
+    int pairs_direct = 0;  // the same for the direct-epilogue pair variant
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -1283,26 +1498,39 @@ DeviceInfo *device_info(int dev) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<1>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
-        d->err = cudaFuncSetAttribute(gemm_tc_kernel<2>,
+        d->err = cudaFuncSetAttribute(gemm_tc_kernel<2, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      Cfg<2>::SMEM_BYTES);
+                                      Cfg<2, false>::SMEM_BYTES);
+        if (d->err != cudaSuccess) return;
+        d->err = cudaFuncSetAttribute(gemm_tc_kernel<2, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<2, true>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
         cudaLaunchAttribute attr;
-        cudaLaunchConfig_t cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2>::SMEM_BYTES, 0, &attr);
+        cudaLaunchConfig_t cfg =
+            launch_config(2 * (d->sms / 2), 2, Cfg<2, false>::SMEM_BYTES, 0, &attr);
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, false>, &cfg) !=
             cudaSuccess) {
             clusters = 0;
             (void)cudaGetLastError();  // clear it: the pair variant is then not used
         }
         d->pairs = clusters;
+        cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, true>::SMEM_BYTES, 0, &attr);
+        clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, true>, &cfg) !=
+            cudaSuccess) {
+            clusters = 0;
+            (void)cudaGetLastError();  // clear it: the direct variant is then not used
+        }
+        d->pairs_direct = clusters;
     });
     return d;
 }
 
-template <int CG>
+template <int CG, bool DIRECT = false>
 cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStream_t stream) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, DIRECT>;
     CUtensorMap map_a, map_b;
     const CUtensorMapDataType dt =
         a0.ab_format == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -1344,7 +1572,7 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr, a.ks > 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG>, map_a, map_b, map_c, map_d, a);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_c, map_d, a);
 }
 
 }  // namespace
@@ -1407,12 +1635,19 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
     // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
     const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
-    if (d->pairs > 0 && pair_tiles >= d->pairs) {
-        *name = bf16 ? "gemm_bf16_tc<pair>" : "gemm_f16_tc<pair>";
+    // beta = 0 and D rows that start on 32 bytes: the direct epilogue (D
+    // from registers, no staging boxes), whose ring is one stage deeper
+    const int64_t d_per_32b = p.d_bf16 ? 16 : 8;
+    const bool direct = p.beta == 0.f && aligned(p.D, 32) && p.ldd % d_per_32b == 0 &&
+                        d->pairs_direct > 0;
+    const int pairs = direct ? d->pairs_direct : d->pairs;
+    if (pairs > 0 && pair_tiles >= pairs) {
+        *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct>" : "gemm_f16_tc<pair,direct>")
+                       : (bf16 ? "gemm_bf16_tc<pair>" : "gemm_f16_tc<pair>");
         // The tiles of the last, partial round would leave pairs idle: when
         // they fill at most half of the pairs, split each into tail_ks K
         // ranges (2 to 4, at least 4 K blocks each) so that round ends sooner.
-        const int64_t groups = d->pairs;
+        const int64_t groups = pairs;
         const int64_t tail = pair_tiles % groups;
         int64_t tail_ks = 1;
         if (tail > 0 && 2 * tail <= groups) {
@@ -1426,7 +1661,9 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         void *ws = nullptr;
         SplitSync sync;  // the stream's split counters, held until the launch is enqueued
         if (tail_ks > 1) {
-            *name = bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>";
+            *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct,split-tail>"
+                                   : "gemm_f16_tc<pair,direct,split-tail>")
+                           : (bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>");
             // counters: per tail tile 2 CTAs x 4 warps (the stream's, zero)
             e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * 4, 0);
             if (e != cudaSuccess) return e;
@@ -1437,7 +1674,8 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
         }
-        e = launch_variant<2>(p, a, 2 * d->pairs, stream);
+        e = direct ? launch_variant<2, true>(p, a, 2 * pairs, stream)
+                   : launch_variant<2, false>(p, a, 2 * pairs, stream);
         if (ws != nullptr) {
             const cudaError_t ef = workspace_free(ws, stream);
             if (e == cudaSuccess) e = ef;

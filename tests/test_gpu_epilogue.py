@@ -129,3 +129,22 @@ def test_epilogue_rejects_bad_descriptors():
     st = lib.gemm_bf16_f32acc_ex(8, 8, 8, 1.0, A, 8, ROW, A, 8, COL, 0.0, None, 8,
                                  Dh.data_ptr() + 2, 9, ROW, d_type=lib.GEMM_D_BF16, check=False)
     assert st == lib.GEMM_OK
+
+
+@pytest.mark.parametrize("variant", ["pair", "pair_tail", "col_major_d"])
+@pytest.mark.parametrize("d_type", DTYPES)
+def test_epilogue_direct_pair_kernel(variant, d_type):
+    """beta = 0 with D rows on 32 bytes: the CTA-pair kernel's direct epilogue
+    (bias, GELU and the BF16 conversion in registers, D stored from them),
+    whole tiles and split tail tiles, ragged N, row- and column-major D."""
+    shapes = {"pair": (2500, 2600, 136), "pair_tail": (2000, 3300, 777),
+              "col_major_d": (2600, 2500, 136)}
+    M, N, K = shapes[variant]
+    order_cd = COL if variant == "col_major_d" else ROW
+    w = Workload("epi_direct_" + variant, M, N, K, 1.5, 0.0, "bf16", ROW, COL, order_cd)
+    inp = make_inputs(w, seed=36, ld_multiple=8)
+    bias = bias_for(w, 37)
+    cols = N if order_cd == ROW else M
+    per32 = 8 if d_type == lib.GEMM_D_F32 else 16  # elements in 32 bytes
+    pad_d = per32 + (-cols) % per32                # ldd on 32 bytes, plus a guard band
+    check(w, inp, bias, lib.GEMM_ACT_GELU, d_type, pad_d=pad_d, expect="gemm_bf16_tc<pair,direct")

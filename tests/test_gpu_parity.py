@@ -165,8 +165,12 @@ def test_cta_pair_variant_small_integers_bit_exact():
     w = Workload("pair_int", 2304, 2560, 1000, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
     inp = make_inputs(w, seed=12)
     Dbuf, _, name = run_gpu(w, inp)
-    assert name.startswith("gemm_bf16_tc<pair")
+    assert name.startswith("gemm_bf16_tc<pair,direct")  # beta = 0, 32-byte rows
     ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
+    # the staged epilogue on the same problem (ldd not a multiple of 8)
+    Dbuf, _, name = run_gpu(w, inp, pad_d=3)
+    assert name.startswith("gemm_bf16_tc<pair") and "direct" not in name, name
     assert np.array_equal(logical_d(w, Dbuf), ref.astype(np.float32))
 
 
@@ -456,3 +460,44 @@ def test_torch_helper_matches_oracle():
     torch.cuda.synchronize()
     ref, S = oracle_full(w, inp)
     assert_within(w, D.cpu().numpy(), ref, S, None)
+
+
+# ---------------------------------------------- the pair kernel's direct epilogue
+# beta = 0 and D rows that start on 32 bytes (ldd a multiple of 8 FP32
+# values): the CTA-pair kernel stores D from registers, with a 7-stage ring.
+def _pad_to_32_bytes(w):
+    cols = w.N if w.order_cd == ROW else w.M
+    return 8 + (-cols) % 8  # ldd a multiple of 8, and a guard band
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_direct_epilogue_pair_all_orders_full(orders):
+    M, N, K = PAIR_SHAPE
+    w = Workload("pair_direct", M, N, K, 1.5, 0.0, "bf16", *orders)
+    inp = make_inputs(w, seed=41, pad=5, ld_multiple=8)
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_direct_epilogue_split_tail_full(shape, dtype):
+    M, N, K = shape
+    w = Workload("tail_direct", M, N, K, 0.75, 0.0, dtype, ROW, COL, ROW)
+    inp = make_inputs(w, seed=42, ld_multiple=8)
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
+    if _pairs_resident() == 76:
+        assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-tail>"
+
+
+def test_direct_epilogue_split_tail_integers_exact_and_deterministic():
+    w = Workload("tail_direct_int", 2048, 3072, 768, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
+    inp = make_inputs(w, seed=43)
+    D1, _, name = run_gpu(w, inp)
+    assert name.startswith("gemm_bf16_tc<pair,direct")
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, D1), ref.astype(np.float32))
+    w = w.with_(dist="normal", alpha=0.5)
+    inp = make_inputs(w, seed=44)
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
