@@ -76,10 +76,10 @@ static_assert(GEMM_TC_DIRECT_STAGES >= 2 && GEMM_TC_DIRECT_STAGES <= 7,
               "the direct pair ring holds 2 to 7 stages");
 
 // DIRECT (CTA pairs only): the epilogue moves each accumulator row from
-// registers straight to D with 32-byte stores, and a split tile's pieces
-// travel the same way, so the kernel needs no staging boxes and the ring
-// takes their shared memory.  For beta = 0 and D rows that start on
-// 32 bytes.
+// registers straight to D with 32-byte stores (and reads C the same way), and
+// a split tile's pieces travel the same way, so the kernel needs no staging
+// boxes and the ring takes their shared memory.  For D (and C, when
+// beta != 0) rows that start on 32 bytes.
 template <int CG, bool DIRECT = false>
 struct Cfg {
     static_assert(!DIRECT || CG == 2, "the direct epilogue is built for CTA pairs");
@@ -550,6 +550,33 @@ __device__ __forceinline__ void ld_global_cg_v8(const float *p, float (&v)[8]) {
                  : "memory");
 }
 
+// Direct epilogue: one lane's 32 values C(row, c0 + j), j < 32, into c
+// (32-byte loads through L2 when the 32 columns are inside the matrix,
+// guarded scalar loads at its edge, zeros past it).  Each element of C is
+// read by the thread that later writes the same element of D, before it
+// does, so C may be D (in-place update).
+__device__ __forceinline__ void load_c_row_direct(const TcArgs &a, int64_t row, int64_t c0,
+                                                  float (&c)[32]) {
+    if (row >= a.M) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) c[j] = 0.f;
+        return;
+    }
+    const float *src = a.C + row * a.ldc + c0;
+    if (c0 + 32 <= a.N) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float v[8];
+            ld_global_cg_v8(src + q * 8, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[q * 8 + j] = v[j];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) c[j] = c0 + j < a.N ? src[j] : 0.f;
+    }
+}
+
 // Direct epilogue: bias, activation and the store of one lane's 32 values
 // o[j] = D(row, c0 + j), from registers straight to D (32-byte stores when
 // the 32 columns are inside the matrix, guarded scalar stores at its edge).
@@ -847,14 +874,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if constexpr (DIRECT) {
         // ------------------------------------------ epilogue warps 2-5, direct
         // Per tile, the warp drains its 32 accumulator rows (TMEM lanes) in
-        // 32-column chunks: tcgen05.ld -> alpha * acc (bias, activation) in
-        // registers -> each lane stores its row's 32 values to D with
-        // 32-byte stores.  beta = 0: C is not read.  A split tile's pieces
+        // 32-column chunks: tcgen05.ld -> alpha * acc + beta * C (bias,
+        // activation) in registers -> each lane stores its row's 32 values
+        // to D with 32-byte stores; each lane loads its row's C with 32-byte
+        // loads, one chunk ahead.  A split tile's pieces
         // publish their raw sums the same way (one 32 x 32 block of rows per
         // warp and chunk) and the last piece adds them, in K order, straight
         // from global memory.
         const int quarter = warp % 4;  // TMEM lanes this warp may access
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool use_c = args.beta != 0.f;
         int64_t li = 0;
         for (int64_t w = group_id; w < n_items; w += num_groups, ++li) {
             const WorkItem it = work_item<CG>(w, args);
@@ -940,12 +969,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
+                    if (use_c) {
+                        float c[32];
+                        load_c_row_direct(args, row, col0 + chunk * 32, c);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = fmaf(args.beta, c[j], o[j]);
+                    }
                     store_row_direct(o, args, row, col0 + chunk * 32);
                 }
                 continue;
             }
+            float c_next[32];  // C of the next chunk, loaded one chunk ahead
+            if (use_c && n_chunks > 0) load_c_row_direct(args, row, col0, c_next);
 #pragma unroll 1
             for (int chunk = 0; chunk < n_chunks; ++chunk) {
+                float c[32];
+                if (use_c) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) c[j] = c_next[j];
+                    if (chunk + 1 < n_chunks)
+                        load_c_row_direct(args, row, col0 + (chunk + 1) * 32, c_next);
+                }
                 uint32_t v[32];
                 __syncwarp();  // tcgen05.ld is warp-collective: converge first
                 tmem_load_32cols(t_acc + chunk * 32, v);
@@ -953,6 +997,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float o[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                if (use_c) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = fmaf(args.beta, c[j], o[j]);
+                }
                 store_row_direct(o, args, row, col0 + chunk * 32);
             }
             if (n_chunks == 0) release_acc();
@@ -1635,10 +1683,12 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
     // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
     const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
-    // beta = 0 and D rows that start on 32 bytes: the direct epilogue (D
-    // from registers, no staging boxes), whose ring is one stage deeper
+    // D rows (and C rows, when beta != 0) that start on 32 bytes: the direct
+    // epilogue (C and D through registers, no staging boxes), whose ring is
+    // one stage deeper
     const int64_t d_per_32b = p.d_bf16 ? 16 : 8;
-    const bool direct = p.beta == 0.f && aligned(p.D, 32) && p.ldd % d_per_32b == 0 &&
+    const bool c_rows_32b = p.beta == 0.f || (aligned(p.C, 32) && p.ldc % 8 == 0);
+    const bool direct = c_rows_32b && aligned(p.D, 32) && p.ldd % d_per_32b == 0 &&
                         d->pairs_direct > 0;
     const int pairs = direct ? d->pairs_direct : d->pairs;
     if (pairs > 0 && pair_tiles >= pairs) {

@@ -78,11 +78,12 @@ def test_epilogue_tensor_core_moderate(act, d_type, with_bias):
     check(w, inp, bias, act, d_type, pad_d=8, expect="gemm_bf16_tc")
 
 
-@pytest.mark.parametrize("variant", ["pair", "pair_tail", "splitk", "simt", "scale_c",
-                                     "col_major_d", "unaligned_d", "ragged_n"])
+@pytest.mark.parametrize("variant", ["pair", "pair_staged", "pair_tail", "splitk", "simt",
+                                     "scale_c", "col_major_d", "unaligned_d", "ragged_n"])
 @pytest.mark.parametrize("d_type", DTYPES)
 def test_epilogue_every_path(variant, d_type):
-    shapes = {"pair": (2500, 2600, 136), "pair_tail": (2000, 3300, 777), "splitk": (300, 600, 2048), "simt": (150, 270, 101),
+    shapes = {"pair": (2500, 2600, 136), "pair_staged": (2500, 2600, 136),
+              "pair_tail": (2000, 3300, 777), "splitk": (300, 600, 2048), "simt": (150, 270, 101),
               "scale_c": (70, 90, 0), "col_major_d": (300, 600, 200), "unaligned_d": (300, 601, 200),
               "ragged_n": (300, 601, 200)}
     M, N, K = shapes[variant]
@@ -90,13 +91,16 @@ def test_epilogue_every_path(variant, d_type):
     w = Workload("epi_" + variant, M, N, K, 1.5, -0.25, "bf16", ROW, COL, order_cd)
     inp = make_inputs(w, seed=33, ld_multiple=1 if variant == "simt" else 8)
     bias = bias_for(w, 34)
-    expect = {"pair": "gemm_bf16_tc<pair>", "pair_tail": "gemm_bf16_tc<pair",
+    expect = {"pair": "gemm_bf16_tc<pair,direct>", "pair_staged": "gemm_bf16_tc<pair>",
+              "pair_tail": "gemm_bf16_tc<pair",
               "splitk": "gemm_bf16_tc<splitk>",
               "simt": "sgemm_simt<bf16", "scale_c": "scale_c", "col_major_d": "gemm_bf16_tc",
               "unaligned_d": "gemm_bf16_tc", "ragged_n": "gemm_bf16_tc"}[variant]
-    # D rows on 16 bytes (TMA store) except: unaligned_d has an odd ldd (603), and
-    # ragged_n a 16-byte ldd (608) but rows of 601 elements (both take row stores)
-    pad_d = {"unaligned_d": 2, "ragged_n": 7}.get(variant, 8)
+    # D rows on 32 bytes (the pair kernel's direct epilogue; TMA stores on the
+    # single-CTA kernel) except: pair_staged has 16-byte rows (2604, staged
+    # boxes and TMA stores), unaligned_d an odd ldd (603), and ragged_n a
+    # 16-byte ldd (608) but rows of 601 elements (both take row stores)
+    pad_d = {"pair_staged": 4, "unaligned_d": 2, "ragged_n": 7}.get(variant, 8)
     check(w, inp, bias, lib.GEMM_ACT_GELU, d_type, pad_d=pad_d, expect=expect)
 
 
@@ -136,7 +140,8 @@ def test_epilogue_rejects_bad_descriptors():
 def test_epilogue_direct_pair_kernel(variant, d_type):
     """beta = 0 with D rows on 32 bytes: the CTA-pair kernel's direct epilogue
     (bias, GELU and the BF16 conversion in registers, D stored from them),
-    whole tiles and split tail tiles, ragged N, row- and column-major D."""
+    whole tiles and split tail tiles, ragged N, row- and column-major D.
+    (beta != 0 with C rows on 32 bytes is covered by test_epilogue_every_path.)"""
     shapes = {"pair": (2500, 2600, 136), "pair_tail": (2000, 3300, 777),
               "col_major_d": (2600, 2500, 136)}
     M, N, K = shapes[variant]

@@ -336,6 +336,19 @@ def test_in_place_c_equals_d(dtype):
     assert_within(w, logical_d(w, Dbuf), ref, S, c_logical(w, inp))
 
 
+@pytest.mark.parametrize("shape", [PAIR_SHAPE, (2000, 3300, 777)])
+def test_in_place_c_equals_d_pair_direct(shape):
+    # the CTA pair's direct epilogue reads C and writes D through registers,
+    # whole tiles and split tail tiles
+    M, N, K = shape
+    w = Workload("inplace_pair", M, N, K, 0.5, 1.0, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=7, ld_multiple=8)
+    Dbuf, _, name = run_gpu(w, inp, in_place=True)
+    assert name.startswith("gemm_bf16_tc<pair,direct"), name
+    ref, S = oracle_full(w, inp)
+    assert_within(w, logical_d(w, Dbuf), ref, S, c_logical(w, inp))
+
+
 def test_bf16_unaligned_operands_use_cuda_core_path():
     """lda not a multiple of 8, and an operand starting 2 bytes off a 16-byte boundary."""
     w = Workload("unal", 150, 270, 101, 1.5, -0.25, "bf16", ROW, COL, ROW)
@@ -501,3 +514,22 @@ def test_direct_epilogue_split_tail_integers_exact_and_deterministic():
     D1, _, _ = run_gpu(w, inp)
     D2, _, _ = run_gpu(w, inp)
     assert torch.equal(D1, D2)
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_direct_epilogue_with_c_all_orders_full(orders):
+    # beta != 0 with C and D rows on 32 bytes: C is read into registers
+    M, N, K = PAIR_SHAPE
+    w = Workload("pair_direct_c", M, N, K, 1.5, -0.25, "bf16", *orders)
+    inp = make_inputs(w, seed=45, pad=5, ld_multiple=8)
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_direct_epilogue_with_c_split_tail_full(dtype):
+    M, N, K = TAIL_SHAPES[0]  # ragged M, N and K
+    w = Workload("tail_direct_c", M, N, K, 0.5, 1.0, dtype, COL, ROW, ROW)
+    inp = make_inputs(w, seed=46, ld_multiple=8)
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
+    if _pairs_resident() == 76:
+        assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-tail>"
