@@ -310,8 +310,9 @@ def barrier(ws, device=None):
             dist.barrier()
 
 
-def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None):
-    """Time the oracle on whole rows of D (bounded sample).  Returns the JSON object."""
+def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None, threads=0):
+    """Time the oracle on whole rows of D (bounded sample) with `threads`
+    host threads (0: one per core).  Returns the JSON object."""
     import numpy as np
     import oracle
 
@@ -326,14 +327,15 @@ def run_cpu_baseline(w, inp, target_s=12.0, max_rows=None):
         return t.numpy().reshape(-1)
 
     A, B, C = bits(inp["A"]), bits(inp["B"]), bits(inp["C"])
-    threads = oracle.default_threads()
+    threads = threads if threads > 0 else oracle.default_threads()
 
     def rows_run(r0, nrows):
         I = np.repeat(np.arange(r0, r0 + nrows, dtype=np.int64), w.N)
         J = np.tile(np.arange(w.N, dtype=np.int64), nrows)
         t0 = time.perf_counter()
         D, S = oracle.gemm_points(w.M, w.N, w.K, w.alpha, A, inp["lda"], w.order_a, B,
-                                  inp["ldb"], w.order_b, w.beta, C, inp["ldc"], w.order_cd, I, J)
+                                  inp["ldb"], w.order_b, w.beta, C, inp["ldc"], w.order_cd, I, J,
+                                  nthreads=threads)
         return time.perf_counter() - t0, D, S
 
     # calibrate on one row per thread, then size the sample to ~target_s
@@ -534,12 +536,12 @@ class Workbench:
         roof["kernel"] = kname
         return roof
 
-    def spot_check(self, target_s):
+    def spot_check(self, target_s, threads=0):
         """The oracle on whole rows of the first copy's D (bounded sample):
         returns (cpu_baseline object, largest |D - D_ref| / bound)."""
         import numpy as np
         w, inp = self.w, self.inp
-        cpu = run_cpu_baseline(w, inp, target_s=target_s)
+        cpu = run_cpu_baseline(w, inp, target_s=target_s, threads=threads)
         rows = cpu.pop("_rows")
         Dref, S = cpu.pop("_D"), cpu.pop("_S")
         D = self.rot[0][3]
@@ -691,7 +693,7 @@ def bench_ours(args):
     cpu = None
     if not args.no_cpu_baseline:
         # the oracle's sample doubles as a parity spot check of the timed output
-        cpu, _ = wb.spot_check(target_s=args.cpu_seconds)
+        cpu, _ = wb.spot_check(target_s=args.cpu_seconds, threads=args.cpu_threads)
 
     line = {
         "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -722,10 +724,10 @@ def bench_reference(args):
     inp = make_inputs(w, seed=0)
     per_step = max(0.5, min(10.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        run_cpu_baseline(w, inp, target_s=per_step)
+        run_cpu_baseline(w, inp, target_s=per_step, threads=args.cpu_threads)
     t_total, flops_total, cores, rows_total = 0.0, 0.0, 0, 0
     for _ in range(args.steps):
-        r = run_cpu_baseline(w, inp, target_s=per_step)
+        r = run_cpu_baseline(w, inp, target_s=per_step, threads=args.cpu_threads)
         t_total += r["seconds"]
         flops_total += 2.0 * r["_rows"] * w.N * w.K
         rows_total += r["_rows"]
@@ -842,7 +844,15 @@ def bench_sweep_stages(args):
 
 
 # ------------------------------------------------------------- peak probes
-NOMINAL_BF16_DENSE_TFLOPS = 2250.0  # NVIDIA's GB300 dense BF16 figure (no sparsity)
+# Dense BF16 tensor-core rate per SM and clock: a 128 x 256 x 16 MMA of one
+# CTA (1,048,576 FLOP) every 128 cycles, 8192 FLOP per cycle per SM.
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def bf16_formula_tflops(sms, mhz):
+    """Dense BF16 tensor peak from the SM count and clock: SMs x 8192 x clock."""
+    return sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+
 
 
 def bench_probe(args):
@@ -895,7 +905,9 @@ def bench_probe(args):
         "tc_bf16_pair": dict(tc2, n_mma=n_mma, mma="256x256x16 per CTA pair"),
         "tc_bf16_single": dict(tc1, n_mma=n_mma, mma="128x256x16 per CTA"),
         "fma_f32": dict(fma, trips=trips),
-        "nominal_bf16_dense_tflops": NOMINAL_BF16_DENSE_TFLOPS,
+        "bf16_formula_tflops": {"at_max_clock": bf16_formula_tflops(sms, max_mhz),
+                                "at_run_clock": bf16_formula_tflops(sms, mhz) if mhz else None,
+                                "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM, "sms": sms},
         "measured_cublas_bf16_tflops": {"burst": peaks.get("bf16_tflops"),
                                         "sustained": peaks.get("bf16_tflops_sustained"),
                                         "source": src},
@@ -919,6 +931,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the oracle (reference arm and CPU baseline); 0: all cores")
     ap.add_argument("--secondary", default=",".join(SECONDARY),
                     help="workloads timed after the headline, each in its own region "
                          "(comma list, or 'none')")

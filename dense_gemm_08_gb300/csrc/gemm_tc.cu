@@ -56,7 +56,6 @@ constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;  // tile width = MMA N
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
-constexpr int NUM_THREADS = 192;          // 6 warps
 constexpr int kGroupM = 16;               // grouped raster width (tile rows)
 
 // Depth of the CTA pair's operand ring (stages of 32 KiB per CTA).  With the
@@ -90,10 +89,15 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES =
         CG == 1 ? 4 : (DIRECT ? GEMM_TC_DIRECT_STAGES : GEMM_TC_PAIR_STAGES);
-    // epilogue staging: per epilogue warp two 32 x 32 FP32 boxes (4 KiB each)
-    static constexpr int STAGING_BYTES = DIRECT ? 0 : 4 * 2 * 32 * 32 * 4;
+    // epilogue warps: eight (two per TMEM lane quarter, one 32 x 32 FP32 box
+    // of 4 KiB each) for the staged CTA pair, whose epilogue is its limit
+    // when K is short; four (two boxes each) otherwise
+    static constexpr int EPI_WARPS = (CG == 2 && !DIRECT) ? 8 : 4;
+    static constexpr int BOXES = EPI_WARPS == 8 ? 1 : 2;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int STAGING_BYTES = DIRECT ? 0 : EPI_WARPS * BOXES * 32 * 32 * 4;
     // ring + staging + barriers + slack for aligning the ring to 1024 bytes
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 512;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -634,9 +638,61 @@ __device__ __forceinline__ void store_row_direct(float (&o)[32], const TcArgs &a
     }
 }
 
+// Staged epilogue: bias, activation, the 32 values of this lane's row into
+// the box (FP32 swizzled, or BF16 rows of 64 bytes), then the box to D (one
+// TMA store, or coalesced row stores when D cannot be described to TMA).
+__device__ __forceinline__ void emit_box_chunk(float (&o)[32], uint8_t *box, int64_t r0,
+                                               int64_t c0, int lane, const TcArgs &args,
+                                               const CUtensorMap *map_d) {
+    if (args.bias != nullptr) {
+        if (args.bias_per_row) {
+            const int64_t r = r0 + lane;
+            const float bv = r < args.M ? args.bias[r] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] += bv;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] += c0 + j < args.N ? args.bias[c0 + j] : 0.f;
+        }
+    }
+    if (args.act != kActNone) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = apply_activation(o[j], args.act);
+    }
+    if (args.d_bf16) {
+        // BF16 box: 32 rows of 64 bytes, unswizzled
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8)
+            *reinterpret_cast<uint4 *>(box + lane * 64 + q8 * 16) =
+                make_uint4(pack_bf16x2(o[q8 * 8 + 0], o[q8 * 8 + 1]),
+                           pack_bf16x2(o[q8 * 8 + 2], o[q8 * 8 + 3]),
+                           pack_bf16x2(o[q8 * 8 + 4], o[q8 * 8 + 5]),
+                           pack_bf16x2(o[q8 * 8 + 6], o[q8 * 8 + 7]));
+    } else {
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4)
+            *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
+                make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
+    }
+    if (args.tma_d) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0)
+            tma_store_2d(map_d, static_cast<int32_t>(c0), static_cast<int32_t>(r0),
+                         smem_addr(box));
+    } else {
+        __syncwarp();
+        if (args.d_bf16)
+            box_store_rows_bf16(box, args, r0, c0, lane);
+        else
+            box_store_rows(box, args, r0, c0, lane);
+        __syncwarp();
+    }
+}
+
 // ------------------------------------------------------------------- kernel
 template <int CG, bool DIRECT = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c,
@@ -647,16 +703,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *ring = smem;
-    uint8_t *staging = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned, 4 warps x 2 x 4 KiB
+    uint8_t *staging = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned epilogue boxes
     uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
     uint64_t *full = bars;                   // [STAGES]  TMA -> MMA (leader counts both CTAs)
     uint64_t *empty = bars + C::STAGES;      // [STAGES]  MMA -> TMA
     uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
     uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
     uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
-    uint64_t *cbar = drain + 1;              // [4 x 2]   C box loaded (epilogue warp, box)
-    uint64_t *pbar = cbar + 8;               // [4]       split-K pieces loaded (epilogue warp)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pbar + 4);
+    uint64_t *cbar = drain + 1;              // [8]       C box loaded (epilogue warp x box)
+    uint64_t *pbar = cbar + 8;               // [8]       split-K pieces loaded (epilogue warp)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pbar + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
@@ -673,11 +729,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(smem_addr(&tfull[b]), 1);
-            mbar_init(smem_addr(&tempty[b]), 4 * CG);  // one arrival per epilogue warp of the group
+            // one arrival per epilogue warp of the group
+            mbar_init(smem_addr(&tempty[b]), C::EPI_WARPS * CG);
         }
         mbar_init(smem_addr(drain), 1);
         for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&cbar[i]), 1);
-        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&pbar[i]), 1);
+        for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&pbar[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1006,6 +1063,222 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (n_chunks == 0) release_acc();
         }
         __syncwarp();
+    } else if constexpr (C::EPI_WARPS == 8) {
+        // -------------------------------------- epilogue warps 2-9, staged, wide
+        // Two warps per TMEM lane quarter (warp % 4), one box each: warp
+        // e = warp - 2 drains the chunks of parity e / 4 of its quarter's 32
+        // accumulator rows, so two chunks of a quarter are in flight at once.
+        // Per chunk: C into the box (TMA, or coalesced row loads) -> tcgen05.ld
+        // -> D = alpha * acc + beta * C in registers -> the box -> one TMA
+        // store (or coalesced row stores when D's pitch cannot be described to
+        // TMA).
+        const int e = warp - 2;
+        const int quarter = warp % 4;  // TMEM lanes this warp may access
+        const int half = e / 4;        // this warp's chunks: half, half + 2, ...
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool use_c = args.beta != 0.f;
+        const bool tma_c = use_c && args.tma_c;
+        uint8_t *box = staging + e * 4096;
+        const uint32_t cb = smem_addr(&cbar[e]);
+        const uint32_t pb = smem_addr(&pbar[e]);
+        uint32_t cphase = 0;  // parity of the box's next C arrival
+        uint32_t pphase = 0;  // parity of the next split-K piece batch
+        bool stop = false;
+        auto emit_chunk = [&](float (&o)[32], int64_t r0, int64_t c0) {
+            emit_box_chunk(o, box, r0, c0, lane, args, &map_d);
+        };
+        auto box_free = [&]() {  // no TMA store still reads the box
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+        };
+        auto load_c = [&](int64_t c0, int64_t r0) {  // the box is free
+            if (tma_c) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(cb, 32 * 32 * 4);
+                    tma_load_2d<CG>(smem_addr(box), &map_c, static_cast<int32_t>(c0),
+                                    static_cast<int32_t>(r0), map_to_rank(cb, rank));
+                }
+            } else {
+                box_load_rows_async(box, args, r0, c0, lane);
+            }
+        };
+        auto wait_c = [&]() -> bool {
+            if (tma_c) {
+                int landed = 1;
+                if (lane == 0) landed = wait_bounded(cb, cphase, abort_flag, args.timeout_ns);
+                landed = __shfl_sync(0xffffffffu, landed, 0);
+                cphase ^= 1u;
+                return landed != 0;
+            }
+            async_copy_wait<0>();
+            __syncwarp();
+            return true;
+        };
+        auto add_c = [&](float (&o)[32]) {
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 c = *reinterpret_cast<const float4 *>(box + box_offset(lane, j4 * 4));
+                o[j4 * 4 + 0] = fmaf(args.beta, c.x, o[j4 * 4 + 0]);
+                o[j4 * 4 + 1] = fmaf(args.beta, c.y, o[j4 * 4 + 1]);
+                o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
+                o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
+            }
+            __syncwarp();  // every lane has read its C before the box is overwritten
+        };
+        int64_t li = 0;
+        for (int64_t w = group_id; w < n_items && !stop; w += num_groups, ++li) {
+            const WorkItem it = work_item<CG>(w, args);
+            const int64_t t = it.t;
+            const int sp = it.sp;
+            const int buf = static_cast<int>(li & 1);
+            const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
+            // lane 0 waits, the warp follows its verdict (keeps the warp converged)
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(smem_addr(&tfull[buf]), acc_phase, abort_flag, args.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_abort(abort_flag);
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            int64_t tm, tn;
+            tile_coords(t, args, tm, tn);
+            const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
+            const int64_t col0 = tn * BN;
+            int n_chunks = 0;  // chunks holding part of D (warp-uniform)
+            if (row0 < args.M) {
+                const int64_t rest = args.N - col0;
+                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+            }
+            // this warp's last chunk (-1: it has none)
+            const int my_last = n_chunks > half ? half + ((n_chunks - 1 - half) / 2) * 2 : -1;
+            const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
+            auto release_acc = [&]() {
+                // accumulator rows read: hand the buffer back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_addr(&tempty[buf]), 0));
+            };
+            if (it.nsp > 1 && n_chunks > 0) {
+                // ---- a split tail tile: publish this warp's chunks of the
+                // piece's raw sums, count the piece per warp; the last piece
+                // to be counted adds the pieces in K order and writes D (no
+                // piece waits for another)
+                auto piece_box = [&](int piece, int chunk) -> float * {
+                    const int64_t slot = ((t - args.tail_first) * it.nsp + piece) * 2 + rank;
+                    return args.ws + ((slot * 4 + quarter) * 8 + chunk) * 1024;
+                };
+                int *const counter = args.ws_count + ((t - args.tail_first) * 2 + rank) * 8 + e;
+#pragma unroll 1
+                for (int chunk = half; chunk < n_chunks; chunk += 2) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_load_32cols(t_acc + chunk * 32, v);
+                    box_free();
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        *reinterpret_cast<uint4 *>(box + box_offset(lane, j4 * 4)) =
+                            make_uint4(v[j4 * 4 + 0], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) bulk_copy_to_global(piece_box(sp, chunk), smem_addr(box), 4096);
+                }
+                release_acc();
+                if (my_last < 0) continue;  // no piece of this tile has chunks for this warp
+                int reduce = 0;
+                if (lane == 0) {
+                    bulk_wait_all();  // the partial sums are in global memory
+                    __threadfence();
+                    const int before = atomicAdd(counter, 1);
+                    reduce = before == it.nsp - 1;
+                    if (reduce) {
+                        *counter = 0;  // all pieces counted: ready for the next call
+                        __threadfence();
+                    }
+                }
+                reduce = __shfl_sync(0xffffffffu, reduce, 0);
+                if (!reduce) continue;
+                // the operand ring is idle: a split piece is its CTA's last work item
+                uint8_t *pieces = ring + e * (C::STAGES * C::STAGE_BYTES / 8);
+#pragma unroll 1
+                for (int chunk = half; chunk < n_chunks && !stop; chunk += 2) {
+                    const int64_t c0 = col0 + chunk * 32;
+                    box_free();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(pb, static_cast<uint32_t>(it.nsp) * 4096);
+                        for (int s2 = 0; s2 < it.nsp; ++s2)
+                            bulk_copy_to_shared(smem_addr(pieces + s2 * 4096), piece_box(s2, chunk),
+                                                4096, pb);
+                    }
+                    if (use_c) load_c(c0, row0);
+                    int got = 1;
+                    if (lane == 0) got = wait_bounded(pb, pphase, abort_flag, args.timeout_ns);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    pphase ^= 1u;
+                    if (!got) {
+                        if (lane == 0) raise_abort(abort_flag);
+                        aborted = stop = true;
+                        break;
+                    }
+                    // sum of the K pieces in K order (the same order on every run)
+                    float o[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
+                    for (int s2 = 0; s2 < it.nsp; ++s2) {
+                        const uint8_t *part = pieces + s2 * 4096;
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 pv =
+                                *reinterpret_cast<const float4 *>(part + box_offset(lane, j4 * 4));
+                            o[j4 * 4 + 0] += pv.x;
+                            o[j4 * 4 + 1] += pv.y;
+                            o[j4 * 4 + 2] += pv.z;
+                            o[j4 * 4 + 3] += pv.w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
+                    if (use_c) {
+                        if (!wait_c()) {
+                            if (lane == 0) raise_abort(abort_flag);
+                            aborted = stop = true;
+                            break;
+                        }
+                        add_c(o);
+                    }
+                    __syncwarp();  // every lane has read the pieces
+                    emit_chunk(o, row0, c0);
+                }
+                continue;
+            }
+#pragma unroll 1
+            for (int chunk = half; chunk < n_chunks; chunk += 2) {
+                const int64_t c0 = col0 + chunk * 32;
+                box_free();
+                if (use_c) load_c(c0, row0);
+                uint32_t v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective: converge first
+                tmem_load_32cols(t_acc + chunk * 32, v);
+                if (chunk == my_last) release_acc();
+                float o[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
+                if (use_c) {
+                    if (!wait_c()) {
+                        if (lane == 0) raise_abort(abort_flag);
+                        aborted = stop = true;
+                        break;
+                    }
+                    add_c(o);
+                }
+                emit_chunk(o, row0, c0);
+            }
+            if (my_last < 0) release_acc();
+        }
+        if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+        __syncwarp();
     } else {
         // ------------------------------------------------- epilogue warps 2-5
         // Per tile, the warp drains its 32 accumulator rows (TMEM lanes) in
@@ -1033,50 +1306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
         // bias, activation, the box, then the box to D (TMA store or rows)
         auto emit_chunk = [&](float (&o)[32], uint8_t *box, int64_t r0, int64_t c0) {
-            if (args.bias != nullptr) {
-                if (args.bias_per_row) {
-                    const int64_t r = r0 + lane;
-                    const float bv = r < args.M ? args.bias[r] : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] += bv;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] += c0 + j < args.N ? args.bias[c0 + j] : 0.f;
-                }
-            }
-            if (args.act != kActNone) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = apply_activation(o[j], args.act);
-            }
-            if (args.d_bf16) {
-                // BF16 box: 32 rows of 64 bytes, unswizzled
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(box + lane * 64 + q8 * 16) =
-                        make_uint4(pack_bf16x2(o[q8 * 8 + 0], o[q8 * 8 + 1]),
-                                   pack_bf16x2(o[q8 * 8 + 2], o[q8 * 8 + 3]),
-                                   pack_bf16x2(o[q8 * 8 + 4], o[q8 * 8 + 5]),
-                                   pack_bf16x2(o[q8 * 8 + 6], o[q8 * 8 + 7]));
-            } else {
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)
-                    *reinterpret_cast<float4 *>(box + box_offset(lane, j4 * 4)) =
-                        make_float4(o[j4 * 4 + 0], o[j4 * 4 + 1], o[j4 * 4 + 2], o[j4 * 4 + 3]);
-            }
-            if (args.tma_d) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0)
-                    tma_store_2d(&map_d, static_cast<int32_t>(c0), static_cast<int32_t>(r0),
-                                 smem_addr(box));
-            } else {
-                __syncwarp();
-                if (args.d_bf16)
-                    box_store_rows_bf16(box, args, r0, c0, lane);
-                else
-                    box_store_rows(box, args, r0, c0, lane);
-                __syncwarp();
-            }
+            emit_box_chunk(o, box, r0, c0, lane, args, &map_d);
         };
         int64_t li = 0;
         for (int64_t w = group_id; w < n_items && !stop; w += num_groups, ++li) {
@@ -1509,11 +1739,11 @@ bool aligned(const void *ptr, size_t bytes) {
 
 // cg = 2: clusters of two CTAs.  cg = 1 and `cooperative`: all CTAs are
 // guaranteed to be resident together (the split-K pieces wait for each other).
-cudaLaunchConfig_t launch_config(int grid, int cg, size_t smem, cudaStream_t stream,
+cudaLaunchConfig_t launch_config(int grid, int cg, int threads, size_t smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr, bool cooperative = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1555,8 +1785,8 @@ DeviceInfo *device_info(int dev) {
                                       Cfg<2, true>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
         cudaLaunchAttribute attr;
-        cudaLaunchConfig_t cfg =
-            launch_config(2 * (d->sms / 2), 2, Cfg<2, false>::SMEM_BYTES, 0, &attr);
+        cudaLaunchConfig_t cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, false>::THREADS,
+                                               Cfg<2, false>::SMEM_BYTES, 0, &attr);
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, false>, &cfg) !=
             cudaSuccess) {
@@ -1564,7 +1794,8 @@ DeviceInfo *device_info(int dev) {
             (void)cudaGetLastError();  // clear it: the pair variant is then not used
         }
         d->pairs = clusters;
-        cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, true>::SMEM_BYTES, 0, &attr);
+        cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, true>::THREADS, Cfg<2, true>::SMEM_BYTES,
+                            0, &attr);
         clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, true>, &cfg) !=
             cudaSuccess) {
@@ -1619,7 +1850,8 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = launch_config(grid, CG, C::SMEM_BYTES, stream, &attr, a.ks > 1);
+    cudaLaunchConfig_t cfg =
+        launch_config(grid, CG, C::THREADS, C::SMEM_BYTES, stream, &attr, a.ks > 1);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_c, map_d, a);
 }
 
@@ -1714,8 +1946,10 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct,split-tail>"
                                    : "gemm_f16_tc<pair,direct,split-tail>")
                            : (bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>");
-            // counters: per tail tile 2 CTAs x 4 warps (the stream's, zero)
-            e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * 4, 0);
+            // counters: per tail tile 2 CTAs x the epilogue warps (the
+            // stream's, zero)
+            const int epi_warps = direct ? Cfg<2, true>::EPI_WARPS : Cfg<2, false>::EPI_WARPS;
+            e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * epi_warps, 0);
             if (e != cudaSuccess) return e;
             a.ws_count = sync.counters;
             // per tail tile and piece: 2 CTAs x 4 warps x 8 boxes of 4 KiB

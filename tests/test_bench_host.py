@@ -190,3 +190,8 @@ def test_committed_pipeline_depth_sweep_refits_to_its_stated_fits():
         assert rms == pytest.approx(float(lit["rms"]), rel=1e-3)
         # the piecewise bound fits the measurements better than the smooth curve
         assert rms < float(sat["rms"])
+
+
+def test_bf16_formula_peak():
+    # 152 SMs x 8192 FLOP per clock x 2070 MHz
+    assert bench.bf16_formula_tflops(152, 2070.0) == pytest.approx(2577.5, abs=0.1)
