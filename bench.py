@@ -158,14 +158,14 @@ def nvml_bus_id(device_index):
 class NvmlSampler:
     """SM clock and clock-event reasons (and, every 8th sample, power) read
     from the driver's NVML library (by ctypes) in a thread, as fast as NVML
-    answers (at most every 0.2 ms), so that a timed region of a few
+    answers (at most every 0.1 ms), so that a timed region of a few
     milliseconds still has samples; rows as ClockSampler's.
     Reads only: NVML query calls, no setting is changed."""
     REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                    0x40: "hw_thermal_slowdown"}
     NVML_CLOCK_SM = 1
 
-    def __init__(self, bus_id, index, period_s=0.0002):
+    def __init__(self, bus_id, index, period_s=0.0001):
         self.bus_id, self.index, self.period = bus_id, index, period_s
         self.rows, self.ok, self._stop = [], False, None
 
@@ -215,6 +215,9 @@ class NvmlSampler:
         if opened is None:
             return self
         self.ok = True
+        # switch between Python threads every 0.1 ms while sampling
+        self._switch = sys.getswitchinterval()
+        sys.setswitchinterval(1e-4)
         self._stop = threading.Event()
         self._thread = threading.Thread(target=self._run, args=opened, daemon=True)
         self._thread.start()
@@ -226,6 +229,7 @@ class NvmlSampler:
             time.sleep(0.02)
             self._stop.set()
             self._thread.join(timeout=5)
+            sys.setswitchinterval(self._switch)
         return False
 
 
@@ -489,11 +493,14 @@ class Workbench:
             names.add(self.step())
             launches += 1
         e1.record(self.stream)
+        # Poll the events' completion for the clock samples' window.  The
+        # sleeps hand the interpreter to the sampler thread, which would
+        # otherwise get it only every switch interval.
         while not e0.query():
-            pass
+            time.sleep(2e-5)
         t0 = time.time()
         while not e1.query():
-            pass
+            time.sleep(2e-5)
         t1 = time.time()
         torch.cuda.synchronize(self.device)
         elapsed_ms = e0.elapsed_time(e1)
