@@ -533,3 +533,45 @@ def test_direct_epilogue_with_c_split_tail_full(dtype):
     full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
     if _pairs_resident() == 76:
         assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-tail>"
+
+
+# ------------------------------------------------ epilogue edge cases of the pair kernel
+def test_direct_epilogue_narrow_n_one_partial_chunk():
+    # 77 x 1 pair tiles of which only 24 columns exist: every chunk is the
+    # partial edge chunk (guarded scalar stores), with and without C
+    for beta in (0.0, -0.25):
+        w = Workload("pair_narrow", 19712, 24, 64, 1.5, beta, "bf16", ROW, COL, ROW)
+        inp = make_inputs(w, seed=47, ld_multiple=8)
+        full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+
+
+def _with_ldc(w, inp, ldc):
+    """inp with C (row-major) stored again at leading dimension ldc; A and B unchanged."""
+    assert w.order_cd == ROW and ldc >= w.N
+    C = torch.zeros((w.M, ldc), dtype=torch.float32)
+    C[:, : w.N] = inp["C_logical"]
+    return dict(inp, C=C, ldc=ldc)
+
+
+@pytest.mark.parametrize("shape", [PAIR_SHAPE, (2000, 3300, 777)])
+def test_in_place_c_equals_d_pair_staged(shape):
+    # C = D with rows that do not start on 16 bytes (ldc = ldd = N + 3): the
+    # wide staged epilogue reads C into a box and writes D from it, whole
+    # tiles and split tail tiles
+    M, N, K = shape
+    w = Workload("inplace_staged", M, N, K, 0.5, 1.0, "bf16", ROW, COL, ROW)
+    inp = _with_ldc(w, make_inputs(w, seed=48, ld_multiple=8), N + 3)
+    Dbuf, _, name = run_gpu(w, inp, in_place=True)
+    assert name.startswith("gemm_bf16_tc<pair") and "direct" not in name, name
+    ref, S = oracle_full(w, inp)
+    assert_within(w, logical_d(w, Dbuf), ref, S, c_logical(w, inp))
+
+
+def test_c_rows_off_32_bytes_take_the_staged_epilogue():
+    # D rows on 32 bytes but C rows only on 16 (ldc = N + 4): the direct
+    # epilogue needs both, so the staged one (TMA C boxes) serves the call
+    M, N, K = PAIR_SHAPE
+    w = Workload("pair_c16", M, N, K, 1.5, -0.25, "bf16", ROW, COL, ROW)
+    inp = _with_ldc(w, make_inputs(w, seed=49, ld_multiple=8), N + 4)  # rows on 16 bytes only
+    assert inp["ldc"] % 8 == 4
+    D, _, _ = full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair>")
