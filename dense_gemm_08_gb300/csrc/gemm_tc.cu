@@ -126,6 +126,10 @@ struct TcArgs {
     // another).
     int64_t tail_first;
     int tail_ks;
+    // CG = 2, tail_split_n: the tail tiles are instead split along N into
+    // tail_ks = 2 halves of BN / 2 columns, each over the whole K range (no
+    // partial sums, no reduction; B comes through map_b_half).
+    int tail_split_n;
     float *ws;
     int *ws_count;      // the stream's split counters: zero between calls
     unsigned *ws_flag;  // CG = 1 split-K: [tile * 4 + warp] = generation once all pieces are in
@@ -429,7 +433,8 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn_major, 
 // whole tiles).  CG = 2: whole tiles, then the split tail tiles.
 struct WorkItem {
     int64_t t, kb_begin, kb_end;
-    int sp, nsp;
+    int sp, nsp;         // K piece sp of nsp (nsp = 1: the whole K range)
+    int n_off, n_width;  // columns [n_off, n_off + n_width) of the tile (BN unless split along N)
 };
 
 template <int CG>
@@ -448,6 +453,15 @@ __device__ __forceinline__ WorkItem work_item(int64_t w, const TcArgs &a) {
         it.t = a.tail_first + r / a.tail_ks;
         it.sp = static_cast<int>(r % a.tail_ks);
         it.nsp = a.tail_ks;
+    }
+    it.n_off = 0;
+    it.n_width = BN;
+    if (CG == 2 && a.tail_split_n && w >= a.tail_first) {
+        // an N half of a tail tile, whole K
+        it.n_off = it.sp * (BN / 2);
+        it.n_width = BN / 2;
+        it.sp = 0;
+        it.nsp = 1;
     }
     it.kb_begin = a.num_kb * it.sp / it.nsp;
     it.kb_end = a.num_kb * (it.sp + 1) / it.nsp;
@@ -695,6 +709,7 @@ template <int CG, bool DIRECT = false>
 __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_b_half,
                         const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_d, const TcArgs args) {
     using C = Cfg<CG, DIRECT>;
@@ -742,6 +757,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                      : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b))
                      : "memory");
+        if (args.tail_split_n && args.b_kmajor)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_half))
+                         : "memory");
         if (args.tma_c)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_c))
                          : "memory");
@@ -773,7 +791,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 int64_t tm, tn;
                 tile_coords(it.t, args, tm, tn);
                 const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
-                const int32_t n0 = static_cast<int32_t>(tn * BN + rank * C::B_ROWS);
+                const int b_rows = it.n_width / CG;  // columns of B this CTA loads
+                const int32_t n0 = static_cast<int32_t>(tn * BN + it.n_off + rank * b_rows);
+                const uint32_t stage_tx = CG * (C::A_BYTES + b_rows * BK * 2);
                 // Serpentine K order: every other work item walks its K blocks
                 // backwards, so the blocks a round of tiles reads last are the
                 // ones the next round (the same tile rows, under the grouped
@@ -795,7 +815,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     const uint32_t sa = ring_base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
                     const int32_t k0 = static_cast<int32_t>(kb * BK);
-                    if (leader) mbar_arrive_expect_tx(fb_local, CG * C::STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
                     if (args.a_kmajor) {
                         tma_load_2d<CG>(sa, &map_a, k0, m0, fb);
                     } else {
@@ -803,9 +823,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                             tma_load_2d<CG>(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
                     }
                     if (args.b_kmajor) {
-                        tma_load_2d<CG>(sb, &map_b, k0, n0, fb);
+                        tma_load_2d<CG>(sb, b_rows == C::B_ROWS ? &map_b : &map_b_half, k0, n0, fb);
                     } else {
-                        for (int i = 0; i < C::B_ROWS / 64; ++i)
+                        for (int i = 0; i < b_rows / 64; ++i)
                             tma_load_2d<CG>(sb + i * 64 * 128, &map_b, n0 + 64 * i, k0, fb);
                     }
                     ++issued;
@@ -839,8 +859,10 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && leader) {
-            const uint32_t idesc =
+            const uint32_t idesc_full =
                 make_idesc(C::TILE_M, BN, !args.a_kmajor, !args.b_kmajor, args.ab_format);
+            const uint32_t idesc_half =
+                make_idesc(C::TILE_M, BN / 2, !args.a_kmajor, !args.b_kmajor, args.ab_format);
             int stage = 0;
             uint32_t phase = 0;
             int64_t li = 0;
@@ -863,6 +885,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 const int64_t kb_end = it.kb_end;
                 const int buf = static_cast<int>(li & 1);
                 const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
+                const uint32_t idesc = it.n_width == BN ? idesc_full : idesc_half;
                 if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
                                   args.timeout_ns)) {
                     raise_abort(abort_flag);
@@ -962,11 +985,12 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             tile_coords(t, args, tm, tn);
             const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
             const int64_t row = row0 + lane;                                 // this lane's row
-            const int64_t col0 = tn * BN;
+            const int64_t col0 = tn * BN + it.n_off;
             int n_chunks = 0;  // chunks holding part of D (warp-uniform)
             if (row0 < args.M) {
                 const int64_t rest = args.N - col0;
-                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+                n_chunks = rest >= it.n_width ? it.n_width / 32
+                                              : static_cast<int>(rest > 0 ? (rest + 31) / 32 : 0);
             }
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
             auto release_acc = [&]() {
@@ -1146,11 +1170,12 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             int64_t tm, tn;
             tile_coords(t, args, tm, tn);
             const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
-            const int64_t col0 = tn * BN;
+            const int64_t col0 = tn * BN + it.n_off;
             int n_chunks = 0;  // chunks holding part of D (warp-uniform)
             if (row0 < args.M) {
                 const int64_t rest = args.N - col0;
-                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+                n_chunks = rest >= it.n_width ? it.n_width / 32
+                                              : static_cast<int>(rest > 0 ? (rest + 31) / 32 : 0);
             }
             // this warp's last chunk (-1: it has none)
             const int my_last = n_chunks > half ? half + ((n_chunks - 1 - half) / 2) * 2 : -1;
@@ -1329,11 +1354,12 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             int64_t tm, tn;
             tile_coords(t, args, tm, tn);
             const int64_t row0 = tm * C::TILE_M + rank * BM + quarter * 32;  // warp's first row
-            const int64_t col0 = tn * BN;
+            const int64_t col0 = tn * BN + it.n_off;
             int n_chunks = 0;  // chunks holding part of D (warp-uniform)
             if (row0 < args.M) {
                 const int64_t rest = args.N - col0;
-                n_chunks = rest >= BN ? BN / 32 : static_cast<int>((rest + 31) / 32);
+                n_chunks = rest >= it.n_width ? it.n_width / 32
+                                              : static_cast<int>(rest > 0 ? (rest + 31) / 32 : 0);
             }
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
             auto release_acc = [&]() {
@@ -1824,6 +1850,12 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
         ok = encode_2d(&map_b, dt, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
+    // tail tiles split along N: a K-major B box of half the rows (an
+    // MN-major B takes one 64-column box of map_b instead of two)
+    CUtensorMap map_b_half = map_b;
+    if (a0.tail_split_n && p.b_kmajor &&
+        !encode_2d(&map_b_half, dt, p.B, p.K, p.N, p.ldb, BK, C::B_ROWS / 2))
+        return cudaErrorInvalidValue;
     // C and D: FP32 row-major M x N; 32 x 32 boxes with the 128-byte swizzle
     CUtensorMap map_c, map_d;
     TcArgs a = a0;
@@ -1852,7 +1884,8 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg =
         launch_config(grid, CG, C::THREADS, C::SMEM_BYTES, stream, &attr, a.ks > 1);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_c, map_d, a);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_b_half, map_c,
+                              map_d, a);
 }
 
 }  // namespace
@@ -1906,6 +1939,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.ks = 1;
     a.tail_first = 0;
     a.tail_ks = 1;
+    a.tail_split_n = 0;
     a.ws = nullptr;
     a.ws_count = nullptr;
     a.ws_flag = nullptr;
@@ -1927,12 +1961,23 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct>" : "gemm_f16_tc<pair,direct>")
                        : (bf16 ? "gemm_bf16_tc<pair>" : "gemm_f16_tc<pair>");
         // The tiles of the last, partial round would leave pairs idle: when
-        // they fill at most half of the pairs, split each into tail_ks K
-        // ranges (2 to 4, at least 4 K blocks each) so that round ends sooner.
+        // they fill at most half of the pairs, split each so that round ends
+        // sooner -- into its two N halves (whole K, no partial sums) when
+        // they fill more than a quarter of the pairs and K is at most
+        // kSplitNMaxKb blocks, else into tail_ks K ranges (2 to 4, at least
+        // 4 K blocks each) whose partial sums the last piece adds.  (Timed on
+        // GB300: at 4096^3 the N halves end the round 6 % sooner; at 8192^3
+        // the two ways take the same time -- N = 128 MMAs move 1.5 x the
+        // operand bytes per FLOP, and the K split's reduction is short
+        // beside a half tile of 64 K blocks.)
+        constexpr int64_t kSplitNMaxKb = 96;
         const int64_t groups = pairs;
         const int64_t tail = pair_tiles % groups;
         int64_t tail_ks = 1;
-        if (tail > 0 && 2 * tail <= groups) {
+        if (tail > 0 && 2 * tail <= groups && 4 * tail > groups && a.num_kb <= kSplitNMaxKb) {
+            tail_ks = 2;
+            a.tail_split_n = 1;
+        } else if (tail > 0 && 2 * tail <= groups) {
             tail_ks = groups / tail;
             if (tail_ks > 4) tail_ks = 4;
             if (tail_ks > a.num_kb / 4) tail_ks = a.num_kb / 4;
@@ -1942,7 +1987,12 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         a.tail_ks = static_cast<int>(tail_ks);
         void *ws = nullptr;
         SplitSync sync;  // the stream's split counters, held until the launch is enqueued
-        if (tail_ks > 1) {
+        if (a.tail_split_n) {
+            *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct,split-n-tail>"
+                                   : "gemm_f16_tc<pair,direct,split-n-tail>")
+                           : (bf16 ? "gemm_bf16_tc<pair,split-n-tail>"
+                                   : "gemm_f16_tc<pair,split-n-tail>");
+        } else if (tail_ks > 1) {
             *name = direct ? (bf16 ? "gemm_bf16_tc<pair,direct,split-tail>"
                                    : "gemm_f16_tc<pair,direct,split-tail>")
                            : (bf16 ? "gemm_bf16_tc<pair,split-tail>" : "gemm_f16_tc<pair,split-tail>");

@@ -47,10 +47,12 @@ def run_ex(w, inp, bias, act, d_type, pad_d=0):
     return got, name
 
 
-def check(w, inp, bias, act, d_type, pad_d=0, expect=None):
+def check(w, inp, bias, act, d_type, pad_d=0, expect=None, staged=False):
     got, name = run_ex(w, inp, bias, act, d_type, pad_d)
     if expect:
         assert name.startswith(expect), name
+    if staged:
+        assert "direct" not in name, name
     x, S = oracle_full(w, inp)  # pre-activation value in double
     y = oracle.epilogue(np.ascontiguousarray(x), bias, act)
     tol = 4e-3 * S + 1e-6
@@ -91,7 +93,7 @@ def test_epilogue_every_path(variant, d_type):
     w = Workload("epi_" + variant, M, N, K, 1.5, -0.25, "bf16", ROW, COL, order_cd)
     inp = make_inputs(w, seed=33, ld_multiple=1 if variant == "simt" else 8)
     bias = bias_for(w, 34)
-    expect = {"pair": "gemm_bf16_tc<pair,direct>", "pair_staged": "gemm_bf16_tc<pair>",
+    expect = {"pair": "gemm_bf16_tc<pair,direct", "pair_staged": "gemm_bf16_tc<pair",
               "pair_tail": "gemm_bf16_tc<pair",
               "splitk": "gemm_bf16_tc<splitk>",
               "simt": "sgemm_simt<bf16", "scale_c": "scale_c", "col_major_d": "gemm_bf16_tc",
@@ -101,7 +103,8 @@ def test_epilogue_every_path(variant, d_type):
     # boxes and TMA stores), unaligned_d an odd ldd (603), and ragged_n a
     # 16-byte ldd (608) but rows of 601 elements (both take row stores)
     pad_d = {"pair_staged": 4, "unaligned_d": 2, "ragged_n": 7}.get(variant, 8)
-    check(w, inp, bias, lib.GEMM_ACT_GELU, d_type, pad_d=pad_d, expect=expect)
+    check(w, inp, bias, lib.GEMM_ACT_GELU, d_type, pad_d=pad_d, expect=expect,
+          staged=variant == "pair_staged")
 
 
 def test_epilogue_null_descriptor_equals_plain_call():

@@ -99,7 +99,8 @@ def test_all_orders_full(dtype, orders):
 
 
 # Big enough for the CTA-pair variant (>= 100 tiles of 256 x 256), ragged in
-# M, N and K, so both CTAs of a pair see partial tiles.
+# M, N and K, so both CTAs of a pair see partial tiles.  With 76 resident
+# pairs its last round holds 34 tiles, each split into two N halves.
 PAIR_SHAPE = (2500, 2600, 136)
 
 
@@ -108,7 +109,8 @@ def test_cta_pair_variant_all_orders_full(orders):
     M, N, K = PAIR_SHAPE
     w = Workload("pair", M, N, K, 1.5, -0.25, "bf16", *orders)
     inp = make_inputs(w, seed=11, pad=5, ld_multiple=8)
-    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair>")
+    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair")
+    assert "direct" not in lib.gemm_last_kernel()
 
 
 # Fewer 128 x 256 tiles than SMs and a long K: the tensor-core kernel splits
@@ -141,7 +143,7 @@ def test_tc_split_k_deterministic_and_exact_on_integers():
 
 @pytest.mark.parametrize("orders", [(ROW, COL, ROW), (COL, ROW, COL)])
 def test_f16_pair_and_split_variants_full(orders):
-    for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair>"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk>")]:
+    for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk>")]:
         M, N, K = shape
         w = Workload("f16var", M, N, K, 1.5, -0.25, "f16", *orders)
         inp = make_inputs(w, seed=22, pad=5, ld_multiple=8)
@@ -175,9 +177,13 @@ def test_cta_pair_variant_small_integers_bit_exact():
 
 
 # The CTA-pair kernel's last round: with 76 resident pairs these shapes leave
-# 28, 20 and 14 tiles for it, which are split into 2, 3 and 4 K ranges; the
-# last piece to finish adds them.  Ragged M, N and K in the first.
+# 28, 20 and 14 tiles for it.  28 and 20 fill more than a quarter of the
+# pairs: each tile is split into its two N halves (whole K, no partial
+# sums); 14 is split into 4 K ranges whose partial sums the last piece to
+# finish adds.  Ragged M, N and K in the first.
 TAIL_SHAPES = [(2000, 3300, 777), (2048, 3072, 768), (2304, 2560, 1024)]
+TAIL_KIND = {TAIL_SHAPES[0]: "split-n-tail", TAIL_SHAPES[1]: "split-n-tail",
+             TAIL_SHAPES[2]: "split-tail"}
 
 
 def _pairs_resident():
@@ -190,6 +196,18 @@ def test_cta_pair_split_tail_all_orders_full(orders):
     w = Workload("pair_tail", M, N, K, 1.5, -0.25, "bf16", *orders)
     inp = make_inputs(w, seed=26, pad=3, ld_multiple=8)
     D, _, _ = full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<pair")
+    if _pairs_resident() == 76:
+        assert lib.gemm_last_kernel() == "gemm_bf16_tc<pair,split-n-tail>"
+
+
+@pytest.mark.parametrize("orders", ORDERS)
+def test_cta_pair_split_k_tail_all_orders_full(orders):
+    M, N, K = TAIL_SHAPES[2]
+    w = Workload("pair_tail_k", M, N - 3, K - 5, 1.5, -0.25, "bf16", *orders)
+    inp = make_inputs(w, seed=28, pad=3, ld_multiple=8)
+    # ldd = 2561 (row-major D) or 2308 (column-major): rows not on 32 bytes,
+    # so the staged epilogue runs
+    full_check(w, inp, pad_d=4, expect_kernel="gemm_bf16_tc<pair")
     if _pairs_resident() == 76:
         assert lib.gemm_last_kernel() == "gemm_bf16_tc<pair,split-tail>"
 
@@ -488,7 +506,7 @@ def test_direct_epilogue_pair_all_orders_full(orders):
     M, N, K = PAIR_SHAPE
     w = Workload("pair_direct", M, N, K, 1.5, 0.0, "bf16", *orders)
     inp = make_inputs(w, seed=41, pad=5, ld_multiple=8)
-    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct")
 
 
 @pytest.mark.parametrize("shape", TAIL_SHAPES)
@@ -499,7 +517,26 @@ def test_direct_epilogue_split_tail_full(shape, dtype):
     inp = make_inputs(w, seed=42, ld_multiple=8)
     full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
     if _pairs_resident() == 76:
-        assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-tail>"
+        assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,{TAIL_KIND[shape]}>"
+
+
+@pytest.mark.parametrize("shape", [TAIL_SHAPES[1], TAIL_SHAPES[2]])
+def test_split_tails_small_integers_exact_and_deterministic(shape):
+    # N-split tail (whole K per half) and K-split tail (partial sums added in
+    # K order): bit-exact on small integers, run to run identical otherwise
+    M, N, K = shape
+    w = Workload("tail_int", M, N, K, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
+    inp = make_inputs(w, seed=50)
+    D1, _, name = run_gpu(w, inp)
+    if _pairs_resident() == 76:
+        assert name == f"gemm_bf16_tc<pair,direct,{TAIL_KIND[shape]}>", name
+    ref, _ = oracle_full(w, inp)
+    assert np.array_equal(logical_d(w, D1), ref.astype(np.float32))
+    w = w.with_(dist="normal", alpha=0.5)
+    inp = make_inputs(w, seed=51)
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
 
 
 def test_direct_epilogue_split_tail_integers_exact_and_deterministic():
@@ -522,7 +559,7 @@ def test_direct_epilogue_with_c_all_orders_full(orders):
     M, N, K = PAIR_SHAPE
     w = Workload("pair_direct_c", M, N, K, 1.5, -0.25, "bf16", *orders)
     inp = make_inputs(w, seed=45, pad=5, ld_multiple=8)
-    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -530,6 +567,16 @@ def test_direct_epilogue_with_c_split_tail_full(dtype):
     M, N, K = TAIL_SHAPES[0]  # ragged M, N and K
     w = Workload("tail_direct_c", M, N, K, 0.5, 1.0, dtype, COL, ROW, ROW)
     inp = make_inputs(w, seed=46, ld_multiple=8)
+    full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
+    if _pairs_resident() == 76:
+        assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-n-tail>"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_direct_epilogue_with_c_split_k_tail_full(dtype):
+    M, N, K = TAIL_SHAPES[2]
+    w = Workload("tail_direct_c_k", M, N, K - 7, 0.5, 1.0, dtype, ROW, ROW, ROW)
+    inp = make_inputs(w, seed=52, ld_multiple=8)
     full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel=f"gemm_{dtype}_tc<pair,direct")
     if _pairs_resident() == 76:
         assert lib.gemm_last_kernel() == f"gemm_{dtype}_tc<pair,direct,split-tail>"
@@ -542,7 +589,7 @@ def test_direct_epilogue_narrow_n_one_partial_chunk():
     for beta in (0.0, -0.25):
         w = Workload("pair_narrow", 19712, 24, 64, 1.5, beta, "bf16", ROW, COL, ROW)
         inp = make_inputs(w, seed=47, ld_multiple=8)
-        full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct>")
+        full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair,direct")
 
 
 def _with_ldc(w, inp, ldc):
@@ -574,4 +621,5 @@ def test_c_rows_off_32_bytes_take_the_staged_epilogue():
     w = Workload("pair_c16", M, N, K, 1.5, -0.25, "bf16", ROW, COL, ROW)
     inp = _with_ldc(w, make_inputs(w, seed=49, ld_multiple=8), N + 4)  # rows on 16 bytes only
     assert inp["ldc"] % 8 == 4
-    D, _, _ = full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair>")
+    D, _, _ = full_check(w, inp, pad_d=_pad_to_32_bytes(w), expect_kernel="gemm_bf16_tc<pair")
+    assert "direct" not in lib.gemm_last_kernel()

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 # (workload, expected kernel prefix)
 CASES = [
     (Workload("tc_splitk", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW), "gemm_bf16_tc<splitk>"),
-    (Workload("pair_tail", 2048, 3072, 768, 0.5, 1.0, "bf16", ROW, COL, ROW), "gemm_bf16_tc<pair"),
+    (Workload("pair_tail", 2304, 2560, 1024, 0.5, 1.0, "bf16", ROW, COL, ROW), "gemm_bf16_tc<pair"),
     (Workload("f16_splitk", 300, 600, 2048, 1.0, 0.5, "f16", COL, ROW, COL), "gemm_f16_tc<splitk>"),
     (Workload("simt_splitk", 384, 384, 1000, 1.5, -0.25, "f32", ROW, ROW, ROW), "sgemm_simt<f32"),
     (Workload("simt_tail", 2560, 2048, 512, 1.0, 0.0, "f32", ROW, COL, ROW), "sgemm_simt<f32"),
