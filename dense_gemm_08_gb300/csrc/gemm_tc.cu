@@ -773,6 +773,10 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // on-chip set-up done: wait for the previous kernel on the stream before
+    // any global memory access, and let the next launch be scheduled
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int64_t n_items = work_items<CG>(args);
     const uint32_t ring_base = smem_addr(ring);
@@ -1764,7 +1768,9 @@ bool aligned(const void *ptr, size_t bytes) {
 }
 
 // cg = 2: clusters of two CTAs.  cg = 1 and `cooperative`: all CTAs are
-// guaranteed to be resident together (the split-K pieces wait for each other).
+// guaranteed to be resident together (the split-K pieces wait for each
+// other).  Other launches may start early (programmatic dependent launch,
+// see pdl_wait).  attr must hold two entries.
 cudaLaunchConfig_t launch_config(int grid, int cg, int threads, size_t smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr, bool cooperative = false) {
     cudaLaunchConfig_t cfg = {};
@@ -1774,16 +1780,19 @@ cudaLaunchConfig_t launch_config(int grid, int cg, int threads, size_t smem, cud
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 0;
+    if (cooperative) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+        attr[cfg.numAttrs].val.cooperative = 1;
+        ++cfg.numAttrs;
+    } else {
+        set_pdl_attribute(&attr[cfg.numAttrs++]);
+    }
     if (cg > 1) {
-        attr->id = cudaLaunchAttributeClusterDimension;
-        attr->val.clusterDim.x = static_cast<unsigned>(cg);
-        attr->val.clusterDim.y = 1;
-        attr->val.clusterDim.z = 1;
-        cfg.numAttrs = 1;
-    } else if (cooperative) {
-        attr->id = cudaLaunchAttributeCooperative;
-        attr->val.cooperative = 1;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(cg);
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
     return cfg;
 }
@@ -1810,9 +1819,11 @@ DeviceInfo *device_info(int dev) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<2, true>::SMEM_BYTES);
         if (d->err != cudaSuccess) return;
-        cudaLaunchAttribute attr;
+        cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, false>::THREADS,
-                                               Cfg<2, false>::SMEM_BYTES, 0, &attr);
+                                               Cfg<2, false>::SMEM_BYTES, 0, attr);
+        cfg.attrs = attr + 1;  // the occupancy query takes the cluster shape only
+        cfg.numAttrs = 1;
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, false>, &cfg) !=
             cudaSuccess) {
@@ -1821,7 +1832,9 @@ DeviceInfo *device_info(int dev) {
         }
         d->pairs = clusters;
         cfg = launch_config(2 * (d->sms / 2), 2, Cfg<2, true>::THREADS, Cfg<2, true>::SMEM_BYTES,
-                            0, &attr);
+                            0, attr);
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
         clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<2, true>, &cfg) !=
             cudaSuccess) {
@@ -1881,9 +1894,9 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     if (!a.tma_d) map_d = map_a;
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
-    cudaLaunchAttribute attr;
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
-        launch_config(grid, CG, C::THREADS, C::SMEM_BYTES, stream, &attr, a.ks > 1);
+        launch_config(grid, CG, C::THREADS, C::SMEM_BYTES, stream, attr, a.ks > 1);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_b_half, map_c,
                               map_d, a);
 }

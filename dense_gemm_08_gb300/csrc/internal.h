@@ -35,6 +35,24 @@ struct Problem {
 
 enum class InType { F32, BF16, F16 };
 
+// Programmatic dependent launch.  The library's kernels are launched with
+// the programmatic-stream-serialization attribute, so a kernel may be
+// scheduled while the kernel before it on the stream is still finishing.
+// Each kernel does its on-chip set-up, then calls pdl_wait() -- which
+// returns once the previous kernel has completed and its memory operations
+// are visible -- before it touches global memory, and pdl_launch_dependents()
+// to let the next launch be scheduled (its CTAs start as this grid's CTAs
+// leave their SMs).  Without a programmatic dependency both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// The launch attribute that allows it.
+inline void set_pdl_attribute(cudaLaunchAttribute *attr) {
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+}
+
 // Temporary device workspace from a library-owned, stream-ordered memory pool
 // (one per device, kept warm between calls): memory handed out on `stream`
 // and returned on `stream` once the kernels enqueued before the free are done.

@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(kThreads) sgemm_cluster_kernel(const ClusterAr
     static_assert(kTile * kTile <= 2 * kTile * kPad, "the partial tile reuses the staging");
     float *as = smem, *bs = smem + kTile * kPad;
 
+    pdl_wait();  // the previous kernel on the stream is done with its memory
+    pdl_launch_dependents();
     const uint32_t rank = cluster_rank();
     const int64_t tile = blockIdx.x / CL;
     const int64_t m0 = (tile / a.tiles_n) * kTile, n0 = (tile % a.tiles_n) * kTile;
@@ -190,13 +192,14 @@ cudaError_t launch_layout(const ClusterArgs &a, unsigned grid, cudaStream_t stre
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CL;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    set_pdl_attribute(&attr[1]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, sgemm_cluster_kernel<CL, AK, BKM>, a);
 }
 

@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_simt_kernel(const Si
     const Problem &p = args.p;
     const T *__restrict__ A = static_cast<const T *>(p.A);
     const T *__restrict__ B = static_cast<const T *>(p.B);
+    pdl_wait();  // the previous kernel on the stream is done with its memory
+    pdl_launch_dependents();
 
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     const int wm = warp / Cfg::WN, wn = warp % Cfg::WN;
@@ -559,16 +561,20 @@ void split_needs(const Problem &p, size_t *part_bytes, size_t *n_counters) {
 // input types are built without it.
 template <typename Cfg, typename T, bool AK, bool BKM>
 cudaError_t launch_kernel(bool epi, unsigned grid, const SimtArgs &args, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl_attribute(&attr[0]);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(Cfg::NT, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (std::is_same<T, uint16_t>::value) {
-        if (epi) {
-            sgemm_simt_kernel<Cfg, T, AK, BKM, true><<<grid, Cfg::NT, 0, stream>>>(args);
-            return cudaSuccess;
-        }
+        if (epi) return cudaLaunchKernelEx(&cfg, sgemm_simt_kernel<Cfg, T, AK, BKM, true>, args);
     } else {
         if (epi) return cudaErrorInvalidValue;
     }
-    sgemm_simt_kernel<Cfg, T, AK, BKM, false><<<grid, Cfg::NT, 0, stream>>>(args);
-    return cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, sgemm_simt_kernel<Cfg, T, AK, BKM, false>, args);
 }
 
 template <typename Cfg, typename T>
@@ -655,6 +661,8 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
 
 __global__ void scale_c_kernel(const Problem p) {
     // D = act(beta * C + bias) (beta may be 0: then C is not read)
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t total = p.M * p.N;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -802,9 +810,17 @@ cudaError_t launch_scale_c(const Problem &p, cudaStream_t stream, const char **n
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    scale_c_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl_attribute(&attr[0]);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, scale_c_kernel, p);
     *name = "scale_c";
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace gemm

@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(kThreads) skinny_bn_kernel(const SkinnyArgs a)
     __shared__ __align__(16) float out[MS * NB];
     const Problem &p = a.p;
     const T *__restrict__ B = static_cast<const T *>(p.B);
+    pdl_wait();  // the previous kernel on the stream is done with its memory
+    pdl_launch_dependents();
     const int64_t cb = blockIdx.x % a.n_cb;
     const int slice = static_cast<int>(blockIdx.x / a.n_cb);
     const int64_t k0 = slice * a.ks;
@@ -297,6 +299,8 @@ __global__ void __launch_bounds__(kThreads) skinny_bk_kernel(const SkinnyArgs a)
     __shared__ __align__(16) float out[MS * NB];
     const Problem &p = a.p;
     const T *__restrict__ B = static_cast<const T *>(p.B);
+    pdl_wait();  // the previous kernel on the stream is done with its memory
+    pdl_launch_dependents();
     const int64_t cb = blockIdx.x % a.n_cb;
     const int slice = static_cast<int>(blockIdx.x / a.n_cb);
     const int64_t k0 = slice * a.ks;
@@ -382,24 +386,26 @@ bool is_aligned(const void *ptr, size_t bytes) {
 }
 
 template <typename T, int MS>
-void launch_ms(const SkinnyArgs &a, unsigned grid, cudaStream_t stream) {
-    if (a.p.b_kmajor)
-        skinny_bk_kernel<T, MS><<<grid, kThreads, 0, stream>>>(a);
-    else
-        skinny_bn_kernel<T, MS><<<grid, kThreads, 0, stream>>>(a);
+cudaError_t launch_ms(const SkinnyArgs &a, unsigned grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl_attribute(&attr[0]);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.p.b_kmajor) return cudaLaunchKernelEx(&cfg, skinny_bk_kernel<T, MS>, a);
+    return cudaLaunchKernelEx(&cfg, skinny_bn_kernel<T, MS>, a);
 }
 
 template <typename T>
-void launch_t(const SkinnyArgs &a, unsigned grid, cudaStream_t stream) {
+cudaError_t launch_t(const SkinnyArgs &a, unsigned grid, cudaStream_t stream) {
     const int64_t M = a.p.M;
-    if (M <= 1)
-        launch_ms<T, 1>(a, grid, stream);
-    else if (M <= 2)
-        launch_ms<T, 2>(a, grid, stream);
-    else if (M <= 4)
-        launch_ms<T, 4>(a, grid, stream);
-    else
-        launch_ms<T, 8>(a, grid, stream);
+    if (M <= 1) return launch_ms<T, 1>(a, grid, stream);
+    if (M <= 2) return launch_ms<T, 2>(a, grid, stream);
+    if (M <= 4) return launch_ms<T, 4>(a, grid, stream);
+    return launch_ms<T, 8>(a, grid, stream);
 }
 
 }  // namespace
@@ -483,17 +489,18 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
         }
     }
     const unsigned g = static_cast<unsigned>(grid);
+    cudaError_t e;
     if (in == InType::F32) {
-        launch_t<float>(a, g, stream);
+        e = launch_t<float>(a, g, stream);
         *name = p.b_kmajor ? "skinny<f32,B:K>" : "skinny<f32,B:N>";
     } else if (in == InType::F16) {
-        launch_t<__half>(a, g, stream);
+        e = launch_t<__half>(a, g, stream);
         *name = p.b_kmajor ? "skinny<f16,B:K>" : "skinny<f16,B:N>";
     } else {
-        launch_t<uint16_t>(a, g, stream);
+        e = launch_t<uint16_t>(a, g, stream);
         *name = p.b_kmajor ? "skinny<bf16,B:K>" : "skinny<bf16,B:N>";
     }
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (ws != nullptr) {
         const cudaError_t ef = workspace_free(ws, stream);
         if (e == cudaSuccess) e = ef;
