@@ -42,6 +42,9 @@ gemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const void 
         return GEMM_ERR_INVALID_VALUE;
     if (!is_order(oa) || !is_order(ob) || !is_order(ocd)) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
+    // a D of more than 2^43 elements exceeds any device's memory (the
+    // kernels' tile indices are 32-bit on that assumption)
+    if (M * N > (int64_t(1) << 43)) return GEMM_ERR_INVALID_VALUE;
     if (D == nullptr || !aligned(D, d_bytes) || ldd < need_ld(ocd, M, N))
         return GEMM_ERR_INVALID_VALUE;
     if (beta != 0.f && (C == nullptr || !aligned(C, sizeof(float)) || ldc < need_ld(ocd, M, N)))

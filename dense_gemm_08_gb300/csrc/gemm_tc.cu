@@ -103,6 +103,23 @@ struct Cfg {
 
 __device__ int g_tc_status;  // 0 = fine, 1 = a bounded wait ran out
 
+// Single-CTA split-K: the K range of a 128 x 256 tile is split over the CTAs
+// of one cluster, at most the largest portable cluster.
+constexpr int kMaxClusterK = 8;
+
+// Shared memory the owner of a split tile's chunks receives the other
+// pieces' chunks in: per lane quarter, (ks - 1) slots of 4 KiB for each of
+// its at most ceil(8 / ks) chunks; the largest over ks = 2..kMaxClusterK.
+constexpr int split_slots_bytes(int ks) { return 4 * (ks - 1) * ((BN / 32 + ks - 1) / ks) * 4096; }
+constexpr int max_split_slots_bytes(int ks = 2) {
+    return ks > kMaxClusterK ? 0
+                             : (split_slots_bytes(ks) > max_split_slots_bytes(ks + 1)
+                                    ? split_slots_bytes(ks)
+                                    : max_split_slots_bytes(ks + 1));
+}
+static_assert(max_split_slots_bytes() <= Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES,
+              "the single-CTA ring holds every split size's receive slots");
+
 struct TcArgs {
     int64_t M, N, K;
     float alpha, beta;
@@ -113,10 +130,8 @@ struct TcArgs {
     int64_t tiles_m, tiles_n, num_kb;
     int a_kmajor, b_kmajor;
     // Split-K (fewer tiles than SMs): work item w is tile w / ks, K blocks
-    // [num_kb * s / ks, num_kb * (s + 1) / ks) with s = w % ks.  Each
-    // epilogue warp publishes its 32-row slab of partial sums in ws (one
-    // 4 KiB box per 32 columns), counts itself in ws_count[tile * 4 + warp];
-    // the last of the ks adds the slabs in K order and writes D.
+    // [num_kb * s / ks, num_kb * (s + 1) / ks) with s = w % ks (see
+    // cluster_k).
     int ks;
     // CTA pairs, last partial round: tiles from tail_first on are split into
     // tail_ks K ranges, one work item each.  Each piece's epilogue warps
@@ -131,9 +146,11 @@ struct TcArgs {
     // partial sums, no reduction; B comes through map_b_half).
     int tail_split_n;
     float *ws;
-    int *ws_count;      // the stream's split counters: zero between calls
-    unsigned *ws_flag;  // CG = 1 split-K: [tile * 4 + warp] = generation once all pieces are in
-    unsigned generation;
+    int *ws_count;  // the stream's split counters: zero between calls
+    // CG = 1 split-K: the ks pieces of a tile are the CTAs of one cluster
+    // (cluster rank = piece), which add their partial sums through
+    // distributed shared memory (no workspace)
+    int cluster_k;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -169,7 +186,19 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// 16 bytes into the shared memory of a CTA of the cluster (address from
+// map_to_rank); a cluster barrier makes them visible to that CTA.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Every thread of every CTA of the cluster; the warp converges first (the
+// .aligned form wants all its lanes at the same instruction).
 __device__ __forceinline__ void cluster_sync() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -437,21 +466,27 @@ struct WorkItem {
     int n_off, n_width;  // columns [n_off, n_off + n_width) of the tile (BN unless split along N)
 };
 
+// Work items and tiles number below 2^31 (the host checks), so the index
+// arithmetic is unsigned 32-bit: a 64-bit division costs several times as
+// much, and the first item's arithmetic lies on the kernel's start-up path.
 template <int CG>
 __device__ __forceinline__ WorkItem work_item(int64_t w, const TcArgs &a) {
     WorkItem it;
+    const uint32_t w32 = static_cast<uint32_t>(w);
     if (CG == 1) {
-        it.t = w / a.ks;
-        it.sp = static_cast<int>(w % a.ks);
+        const uint32_t ks = static_cast<uint32_t>(a.ks);
+        it.t = w32 / ks;
+        it.sp = static_cast<int>(w32 % ks);
         it.nsp = a.ks;
     } else if (w < a.tail_first) {
         it.t = w;
         it.sp = 0;
         it.nsp = 1;
     } else {
-        const int64_t r = w - a.tail_first;
-        it.t = a.tail_first + r / a.tail_ks;
-        it.sp = static_cast<int>(r % a.tail_ks);
+        const uint32_t r = w32 - static_cast<uint32_t>(a.tail_first);
+        const uint32_t tks = static_cast<uint32_t>(a.tail_ks);
+        it.t = a.tail_first + r / tks;
+        it.sp = static_cast<int>(r % tks);
         it.nsp = a.tail_ks;
     }
     it.n_off = 0;
@@ -463,8 +498,10 @@ __device__ __forceinline__ WorkItem work_item(int64_t w, const TcArgs &a) {
         it.sp = 0;
         it.nsp = 1;
     }
-    it.kb_begin = a.num_kb * it.sp / it.nsp;
-    it.kb_end = a.num_kb * (it.sp + 1) / it.nsp;
+    // num_kb < 2^25 (K < 2^31), times a piece index below 8
+    const uint32_t nkb = static_cast<uint32_t>(a.num_kb), nsp = static_cast<uint32_t>(it.nsp);
+    it.kb_begin = nkb * static_cast<uint32_t>(it.sp) / nsp;
+    it.kb_end = nkb * static_cast<uint32_t>(it.sp + 1) / nsp;
     return it;
 }
 
@@ -476,12 +513,15 @@ __device__ __forceinline__ int64_t work_items(const TcArgs &a) {
 
 __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t &tm,
                                             int64_t &tn) {
-    const int64_t width = kGroupM * a.tiles_n;
-    const int64_t first_m = (t / width) * kGroupM;
-    const int64_t rest = a.tiles_m - first_m;
-    const int64_t gsz = rest < kGroupM ? rest : kGroupM;
-    tm = first_m + (t % width) % gsz;
-    tn = (t % width) / gsz;
+    const uint32_t t32 = static_cast<uint32_t>(t);
+    const uint32_t width = kGroupM * static_cast<uint32_t>(a.tiles_n);
+    const uint32_t group = t32 / width, in_group = t32 - group * width;
+    const uint32_t first_m = group * kGroupM;
+    const uint32_t rest = static_cast<uint32_t>(a.tiles_m) - first_m;
+    const uint32_t gsz = rest < static_cast<uint32_t>(kGroupM) ? rest : kGroupM;
+    const uint32_t q = in_group / gsz;
+    tm = first_m + (in_group - q * gsz);
+    tn = q;
 }
 
 // ---------------------------------------------------------- epilogue boxes
@@ -493,6 +533,15 @@ __device__ __forceinline__ void tile_coords(int64_t t, const TcArgs &a, int64_t 
 // CU_TENSOR_MAP_SWIZZLE_128B uses the same layout.
 __device__ __forceinline__ uint32_t box_offset(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ (r & 7))) << 4) + (c & 3) * 4);
+}
+
+// A split-K slot holds a 32 x 32 FP32 chunk with columns 4 * j4 .. 4 * j4 + 3
+// of row r at byte j4 * 512 + r * 16: the warp's 16-byte store (or load) of
+// one j4 covers 512 contiguous bytes, which the cluster's shared-memory
+// network moves in a few wide transfers (a row-per-lane layout would make
+// each lane's 16 bytes a transfer of its own).
+__device__ __forceinline__ uint32_t slot_offset(int r, int j4) {
+    return static_cast<uint32_t>(j4 * 512 + r * 16);
 }
 
 // Start copying C[row0 + rr, c0 + lane], rr < 32, into the box with 4-byte
@@ -860,6 +909,10 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             aborted = !ok;
         }
         __syncwarp();
+        if (CG == 1 && args.cluster_k) {
+            cluster_sync();  // the epilogue warps' (A): operand rings idle
+            cluster_sync();  // their (C): pieces delivered
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && leader) {
@@ -955,6 +1008,10 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             aborted = !ok;
         }
         __syncwarp();
+        if (CG == 1 && args.cluster_k) {
+            cluster_sync();  // the epilogue warps' (A) and (C)
+            cluster_sync();
+        }
     } else if constexpr (DIRECT) {
         // ------------------------------------------ epilogue warps 2-5, direct
         // Per tile, the warp drains its 32 accumulator rows (TMEM lanes) in
@@ -1324,8 +1381,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
         const uint32_t cbar0 = smem_addr(&cbar[quarter * 2]);
         uint32_t nb = 0;      // boxes used so far (box nb & 1 is next)
         uint32_t cphase = 0;  // bit b: parity of box b's next C arrival
-        uint32_t pphase = 0;  // parity of the next split-K piece batch
         bool stop = false;
+        int cluster_bars = 0;  // cluster barriers passed (split pieces pass two)
         auto issue_c = [&](int b, int64_t c0, int64_t r0) {
             // lane 0 only; box b is free (no store still reading it)
             const uint32_t bar = cbar0 + 8 * b;
@@ -1378,128 +1435,82 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                         mbar_arrive_cluster(map_to_rank(te, 0));
                 }
             };
-            if (it.nsp > 1 && n_chunks > 0) {
-                // ---- a split tile.  1) publish this piece's partial sums
-                // (raw accumulator boxes) to ws and count the piece.
-                //   CG = 1: all ks pieces of a tile run at once (cooperative
-                //     launch); once all are counted, piece sp reduces chunks
-                //     sp, sp + ks, ... of the slab -- the chunks of a slab are
-                //     reduced in parallel by different CTAs.
-                //   CG = 2: the last piece to be counted reduces every chunk;
-                //     no piece waits for another.
-                // Either way the pieces are added in K order, so the result
-                // does not depend on which CTA reduces.
-                auto piece_box = [&](int piece, int chunk) -> float * {
-                    const int64_t slot =
-                        CG == 1 ? t * it.nsp + piece
-                                : ((t - args.tail_first) * it.nsp + piece) * 2 + rank;
-                    return args.ws + ((slot * 4 + quarter) * 8 + chunk) * 1024;
+            if (it.nsp > 1) {
+                // ---- a split tile (single CTAs): the ks pieces of the tile
+                // are the CTAs of one thread-block cluster, piece = cluster
+                // rank = K range.  Chunk c (32 columns) belongs to rank c % ks.
+                // A) cluster barrier: every piece's MMAs are done, so every
+                //    CTA's operand ring is idle (a piece is its CTA's only
+                //    work item);
+                // B) each piece stores the chunks it does not own, from TMEM,
+                //    into their owner's ring, one slot per (owned chunk,
+                //    sender) (plain remote stores: nothing waits on them one
+                //    by one);
+                // C) cluster barrier: every slot is written and visible, and
+                //    no CTA touches another's shared memory after it;
+                // D) the owner adds the ks pieces in rank (K) order -- its own
+                //    straight from TMEM -- so the sum does not depend on
+                //    timing, and runs the epilogue.
+                const int ks = it.nsp;
+                const int own_max = (BN / 32 + ks - 1) / ks;  // owned chunks per rank, at most
+                auto slot = [&](int j, int s2) -> uint32_t {  // owned chunk j, sender s2
+                    const int idx = s2 < sp ? s2 : s2 - 1;
+                    return ring_base +
+                           static_cast<uint32_t>(((quarter * own_max + j) * (ks - 1) + idx) * 4096);
                 };
-                int *const counter =
-                    args.ws_count + (CG == 1 ? t * 4 + quarter
-                                             : ((t - args.tail_first) * 2 + rank) * 4 + quarter);
-                unsigned *const flag = args.ws_flag + t * 4 + quarter;  // CG = 1 only
+                cluster_sync();  // (A)
+                ++cluster_bars;
 #pragma unroll 1
                 for (int chunk = 0; chunk < n_chunks; ++chunk) {
-                    uint8_t *box = boxes + (nb & 1) * 4096;
+                    const int owner = chunk % ks;
+                    if (owner == sp) continue;
                     uint32_t v[32];
-                    __syncwarp();
+                    __syncwarp();  // tcgen05.ld is warp-collective: converge first
                     tmem_load_32cols(t_acc + chunk * 32, v);
-                    if (lane == 0) bulk_wait_read<1>();  // the copy that used this box has read it
-                    __syncwarp();
+                    // the owner's slot for this chunk and this sender
+                    const int idx = sp < owner ? sp : sp - 1;
+                    const uint32_t dst_local = ring_base + static_cast<uint32_t>(
+                        ((quarter * own_max + chunk / ks) * (ks - 1) + idx) * 4096);
+                    const uint32_t dst = map_to_rank(dst_local, static_cast<uint32_t>(owner));
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4)
-                        *reinterpret_cast<uint4 *>(box + box_offset(lane, j4 * 4)) =
-                            make_uint4(v[j4 * 4 + 0], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) bulk_copy_to_global(piece_box(sp, chunk), smem_addr(box), 4096);
-                    ++nb;
+                        st_cluster_v4(dst + slot_offset(lane, j4), v[j4 * 4 + 0], v[j4 * 4 + 1],
+                                      v[j4 * 4 + 2], v[j4 * 4 + 3]);
                 }
-                release_acc();  // the rest works from the published boxes
-                int ok2 = 1, reduce = 1;
-                if (lane == 0) {
-                    bulk_wait_all();  // the partial sums are in global memory
-                    __threadfence();
-                    const int before = atomicAdd(counter, 1);
-                    const bool last_in = before == it.nsp - 1;
-                    if (last_in) *counter = 0;  // all pieces counted: ready for the next call
-                    if (CG == 1) {
-                        // 2) wait until all ks pieces are published (all
-                        // resident: one CTA per SM, cooperative launch); the
-                        // last one to be counted raises the tile's flag to
-                        // this call's generation
-                        if (last_in) {
-                            __threadfence();
-                            atomicExch(flag, args.generation);
-                        }
-                        reduce = sp < n_chunks;
-                        if (reduce && !last_in) {
-                            const volatile unsigned *fl = flag;
-                            const uint64_t t0 = global_timer();
-                            while (*fl != args.generation) {
-                                if (*abort_flag || global_timer() - t0 > args.timeout_ns) {
-                                    ok2 = 0;
-                                    break;
-                                }
-                                __nanosleep(64);
-                            }
-                        }
-                    } else {
-                        reduce = last_in;  // the last piece reduces
-                    }
-                    if (reduce) __threadfence();
-                }
-                ok2 = __shfl_sync(0xffffffffu, ok2, 0);
-                reduce = __shfl_sync(0xffffffffu, reduce, 0);
-                if (!ok2) {
-                    if (lane == 0) raise_abort(abort_flag);
-                    aborted = stop = true;
-                    break;
-                }
-                if (!reduce) continue;
-                // the operand ring is idle: a split piece is its CTA's last work item
-                uint8_t *pieces = ring + quarter * (C::STAGES * C::STAGE_BYTES / 4);
-                const int first_chunk = CG == 1 ? sp : 0;
-                const int chunk_step = CG == 1 ? it.nsp : 1;
+                cluster_sync();  // (C)
+                ++cluster_bars;
 #pragma unroll 1
-                for (int chunk = first_chunk; chunk < n_chunks && !stop; chunk += chunk_step) {
+                for (int chunk = sp; chunk < n_chunks && !stop; chunk += ks) {
                     const int b = nb & 1;
                     uint8_t *box = boxes + b * 4096;
                     const int64_t c0 = col0 + chunk * 32;
-                    // all pieces of this chunk, and C, in flight together
-                    if (lane == 0) {
-                        bulk_wait_read<0>();  // no store still reads this box
-                        const uint32_t bar = smem_addr(&pbar[quarter]);
-                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(it.nsp) * 4096);
-                        for (int s2 = 0; s2 < it.nsp; ++s2)
-                            bulk_copy_to_shared(smem_addr(pieces + s2 * 4096), piece_box(s2, chunk),
-                                                4096, bar);
-                        if (tma_c) issue_c(b, c0, row0);
+                    if (use_c) {
+                        if (lane == 0) bulk_wait_read<0>();  // no store still reads this box
+                        __syncwarp();
+                        if (tma_c) {
+                            if (lane == 0) issue_c(b, c0, row0);
+                        } else {
+                            box_load_rows_async(box, args, row0, c0, lane);
+                        }
                     }
+                    uint32_t v[32];
                     __syncwarp();
-                    if (use_c && !tma_c) box_load_rows_async(box, args, row0, c0, lane);
-                    int got = 1;
-                    if (lane == 0)
-                        got = wait_bounded(smem_addr(&pbar[quarter]), pphase, abort_flag,
-                                           args.timeout_ns);
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    pphase ^= 1u;
-                    if (!got) {
-                        if (lane == 0) raise_abort(abort_flag);
-                        aborted = stop = true;
-                        break;
-                    }
-                    // sum of the K pieces in K order (the same order on every run)
+                    tmem_load_32cols(t_acc + chunk * 32, v);
+                    // the ks pieces in rank order (the same order on every run)
                     float o[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = 0.f;
-                    for (int s2 = 0; s2 < it.nsp; ++s2) {
-                        const uint8_t *part = pieces + s2 * 4096;
+                    for (int s2 = 0; s2 < ks; ++s2) {
+                        if (s2 == sp) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] += __uint_as_float(v[j]);
+                            continue;
+                        }
+                        const uint8_t *src = ring + (slot(chunk / ks, s2) - ring_base);
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const float4 pv =
-                                *reinterpret_cast<const float4 *>(part + box_offset(lane, j4 * 4));
+                                *reinterpret_cast<const float4 *>(src + slot_offset(lane, j4));
                             o[j4 * 4 + 0] += pv.x;
                             o[j4 * 4 + 1] += pv.y;
                             o[j4 * 4 + 2] += pv.z;
@@ -1534,11 +1545,14 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                             o[j4 * 4 + 2] = fmaf(args.beta, c.z, o[j4 * 4 + 2]);
                             o[j4 * 4 + 3] = fmaf(args.beta, c.w, o[j4 * 4 + 3]);
                         }
+                    } else {
+                        if (lane == 0) bulk_wait_read<1>();  // the store that used this box has read it
                     }
-                    __syncwarp();  // every lane has read the pieces and C
+                    __syncwarp();  // every lane has read C before the box is overwritten
                     emit_chunk(o, box, row0, c0);
                     ++nb;
                 }
+                release_acc();
                 continue;
             }
             if (use_c && n_chunks > 0) {
@@ -1614,6 +1628,10 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             }
             if (n_chunks == 0) release_acc();
         }
+        // every thread of a split cluster passes both cluster barriers, on
+        // every path (the other CTAs wait there)
+        if (args.cluster_k)
+            for (; cluster_bars < 2; ++cluster_bars) cluster_sync();
         if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
         __syncwarp();
     }
@@ -1754,12 +1772,17 @@ bool encode_box32_f32(CUtensorMap *map, const void *base, int64_t M, int64_t N, 
 
 constexpr int kMaxDevices = 64;
 
+
 struct DeviceInfo {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     int sms = 1;
     int pairs = 0;         // CTA pairs that can be resident at once (0: pair variant not used)
     int pairs_direct = 0;  // the same for the direct-epilogue pair variant
+    // clusters of k single CTAs that can be resident at once, k = 2..8
+    // (-1: not asked yet); asked under `mu`
+    int clusters[kMaxClusterK + 1] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    std::mutex mu;
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -1767,12 +1790,11 @@ bool aligned(const void *ptr, size_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) % bytes) == 0;
 }
 
-// cg = 2: clusters of two CTAs.  cg = 1 and `cooperative`: all CTAs are
-// guaranteed to be resident together (the split-K pieces wait for each
-// other).  Other launches may start early (programmatic dependent launch,
-// see pdl_wait).  attr must hold two entries.
+// A launch of `grid` CTAs in clusters of cg (cg = 1: no cluster), allowed to
+// start early (programmatic dependent launch, see pdl_wait).  attr must hold
+// two entries: [0] the dependent-launch attribute, [1] the cluster shape.
 cudaLaunchConfig_t launch_config(int grid, int cg, int threads, size_t smem, cudaStream_t stream,
-                                 cudaLaunchAttribute *attr, bool cooperative = false) {
+                                 cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
@@ -1780,13 +1802,7 @@ cudaLaunchConfig_t launch_config(int grid, int cg, int threads, size_t smem, cud
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 0;
-    if (cooperative) {
-        attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
-        attr[cfg.numAttrs].val.cooperative = 1;
-        ++cfg.numAttrs;
-    } else {
-        set_pdl_attribute(&attr[cfg.numAttrs++]);
-    }
+    set_pdl_attribute(&attr[cfg.numAttrs++]);
     if (cg > 1) {
         attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
         attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(cg);
@@ -1846,6 +1862,28 @@ DeviceInfo *device_info(int dev) {
     return d;
 }
 
+// How many clusters of k single-CTA tensor-core kernels (each holding most of
+// an SM's shared memory) the device can hold at once; asked once per k.  A
+// cluster's CTAs must share a GPC, so this is below SMs / k when k does not
+// divide a GPC's SM count.
+int resident_clusters(DeviceInfo *d, int k) {
+    std::lock_guard<std::mutex> lock(d->mu);
+    if (d->clusters[k] < 0) {
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg =
+            launch_config(k * (d->sms / k), k, Cfg<1>::THREADS, Cfg<1>::SMEM_BYTES, 0, attr);
+        cfg.attrs = attr + 1;  // the occupancy query takes the cluster shape only
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<1, false>, &cfg) != cudaSuccess) {
+            n = 0;
+            (void)cudaGetLastError();
+        }
+        d->clusters[k] = n;
+    }
+    return d->clusters[k];
+}
+
 template <int CG, bool DIRECT = false>
 cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStream_t stream) {
     using C = Cfg<CG, DIRECT>;
@@ -1895,8 +1933,9 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     a.tiles_m = (p.M + C::TILE_M - 1) / C::TILE_M;
     a.tiles_n = (p.N + BN - 1) / BN;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        launch_config(grid, CG, C::THREADS, C::SMEM_BYTES, stream, attr, a.ks > 1);
+    // CTA pairs: clusters of 2; split single CTAs: clusters of ks
+    const int cluster = CG == 2 ? 2 : (a.cluster_k ? a.ks : 1);
+    cudaLaunchConfig_t cfg = launch_config(grid, cluster, C::THREADS, C::SMEM_BYTES, stream, attr);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, DIRECT>, map_a, map_b, map_b_half, map_c,
                               map_d, a);
 }
@@ -1955,13 +1994,17 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.tail_split_n = 0;
     a.ws = nullptr;
     a.ws_count = nullptr;
-    a.ws_flag = nullptr;
-    a.generation = 0;
+    a.cluster_k = 0;
     a.ab_format = bf16 ? 1 : 0;
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
     // pairs (large problems); single CTAs on 128 x 256 tiles otherwise.
     const int64_t pair_tiles = ((p.M + 255) / 256) * ((p.N + BN - 1) / BN);
+    // The kernel's work-item arithmetic is 32-bit: at most 2^28 tiles of
+    // 128 x 256 (a D of 2^43 elements, beyond any device's memory), times at
+    // most 8 pieces each.
+    if (((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN) > (int64_t(1) << 28))
+        return cudaErrorInvalidValue;
     // D rows (and C rows, when beta != 0) that start on 32 bytes: the direct
     // epilogue (C and D through registers, no staging boxes), whose ring is
     // one stage deeper
@@ -2012,7 +2055,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             // counters: per tail tile 2 CTAs x the epilogue warps (the
             // stream's, zero)
             const int epi_warps = direct ? Cfg<2, true>::EPI_WARPS : Cfg<2, false>::EPI_WARPS;
-            e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * epi_warps, 0);
+            e = sync.acquire(stream, static_cast<size_t>(tail) * 2 * epi_warps);
             if (e != cudaSuccess) return e;
             a.ws_count = sync.counters;
             // per tail tile and piece: 2 CTAs x 4 warps x 8 boxes of 4 KiB
@@ -2031,46 +2074,38 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         if (e == cudaSuccess) e = er;
     } else {
         const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-        // Fewer tiles than SMs: split each tile's K range over ks CTAs
-        // ("GEMM on NVIDIA GPUs", section 5, split-K for short M / N).
+        // Fewer tiles than SMs: split each tile's K range over the ks CTAs
+        // of a cluster ("GEMM on NVIDIA GPUs", section 5, split-K for short
+        // M / N), at most kMaxClusterK (the portable cluster size) and at
+        // least 4 K blocks per piece; the pieces add their partial sums
+        // through distributed shared memory, so no workspace is taken.  The
+        // largest such ks whose clusters (one per tile) are all resident at
+        // once: a second wave of clusters would double the time.
         int64_t ks = 1;
         if (tiles < d->sms) {
             ks = d->sms / tiles;
-            if (ks > a.num_kb / 4) ks = a.num_kb / 4;  // at least 4 K blocks per piece
-            // a reducing piece gathers the ks boxes of a chunk in its warp's
-            // quarter of the operand ring
-            const int64_t fit = static_cast<int64_t>(Cfg<1>::STAGES) * Cfg<1>::STAGE_BYTES / 4 / 4096;
-            if (ks > fit) ks = fit;
+            if (ks > a.num_kb / 4) ks = a.num_kb / 4;
+            if (ks > kMaxClusterK) ks = kMaxClusterK;
+            while (ks >= 2 && resident_clusters(d, static_cast<int>(ks)) < tiles) --ks;
             if (ks < 2) ks = 1;
         }
-        void *ws = nullptr;
-        SplitSync sync;  // the stream's split counters and flags, held until enqueued
         if (ks > 1) {
-            // counters and flags: per tile 4 warps (the stream's: counters
-            // zero, flags other than this call's generation)
-            e = sync.acquire(stream, static_cast<size_t>(tiles) * 4, static_cast<size_t>(tiles) * 4);
-            if (e != cudaSuccess) return e;
-            a.ws_count = sync.counters;
-            a.ws_flag = sync.flags;
-            a.generation = sync.generation;
-            const size_t part_bytes = static_cast<size_t>(tiles) * ks * 4 * 8 * 4096;
-            e = workspace_alloc(part_bytes, stream, &ws);
-            if (e != cudaSuccess) return e;
-            a.ws = static_cast<float *>(ws);
+            static const char *const kNames[2][kMaxClusterK + 1] = {
+                {"", "", "gemm_f16_tc<splitk,x2>", "gemm_f16_tc<splitk,x3>", "gemm_f16_tc<splitk,x4>",
+                 "gemm_f16_tc<splitk,x5>", "gemm_f16_tc<splitk,x6>", "gemm_f16_tc<splitk,x7>",
+                 "gemm_f16_tc<splitk,x8>"},
+                {"", "", "gemm_bf16_tc<splitk,x2>", "gemm_bf16_tc<splitk,x3>",
+                 "gemm_bf16_tc<splitk,x4>", "gemm_bf16_tc<splitk,x5>", "gemm_bf16_tc<splitk,x6>",
+                 "gemm_bf16_tc<splitk,x7>", "gemm_bf16_tc<splitk,x8>"}};
             a.ks = static_cast<int>(ks);
-            *name = bf16 ? "gemm_bf16_tc<splitk>" : "gemm_f16_tc<splitk>";
+            a.cluster_k = 1;
+            *name = kNames[bf16 ? 1 : 0][ks];  // xN: the K range split over N CTAs
         } else {
             *name = bf16 ? "gemm_bf16_tc" : "gemm_f16_tc";
         }
         const int64_t items = tiles * ks;
         const int grid = static_cast<int>(items < d->sms ? items : d->sms);
         e = launch_variant<1>(p, a, grid, stream);
-        if (ws != nullptr) {
-            const cudaError_t ef = workspace_free(ws, stream);
-            if (e == cudaSuccess) e = ef;
-        }
-        const cudaError_t er = sync.release();
-        if (e == cudaSuccess) e = er;
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

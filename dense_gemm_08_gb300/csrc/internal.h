@@ -58,39 +58,34 @@ inline void set_pdl_attribute(cudaLaunchAttribute *attr) {
 // and returned on `stream` once the kernels enqueued before the free are done.
 cudaError_t workspace_alloc(size_t bytes, cudaStream_t stream, void **ptr);
 cudaError_t workspace_free(void *ptr, cudaStream_t stream);
-// The split kernels' counters and flags for one launch on `stream` (current
-// device): after acquire, `counters` has at least n_counters ints that are
-// zero and `flags` at least n_flags unsigned flags that differ from
-// `generation`, the number this launch writes to a flag.
-//   Eager calls get the stream's persistent buffers and enqueue nothing
-//   (except when the buffers grow): every kernel returns the counters it used
+// The split kernels' counters for one launch on `stream` (current device):
+// after acquire, `counters` has at least n_counters ints that are zero.
+//   Eager calls get the stream's persistent buffer and enqueue nothing
+//   (except when the buffer grows): every kernel returns the counters it used
 //   to zero, and calls on one stream run in order, so they may share them
 //   (other streams have their own).  The stream's entry stays held until
-//   release(), which the caller invokes once its launch is enqueued; so the
-//   launches of one stream are enqueued in generation order, from any number
-//   of host threads.
+//   release(), which the caller invokes once its launch is enqueued, so an
+//   outgrown buffer is freed after every launch given it, whichever host
+//   threads make the calls.
 //   Under stream capture a graph may be replayed on any stream, at the same
-//   time as other work, with the generation fixed at capture: the call gets a
-//   fresh zeroed block of graph memory instead (generation 1), freed in
-//   stream order by release().
+//   time as other work: the call gets a fresh zeroed block of graph memory
+//   instead, freed in stream order by release().
 class SplitSync {
    public:
     SplitSync() = default;
     SplitSync(const SplitSync &) = delete;
     SplitSync &operator=(const SplitSync &) = delete;
     ~SplitSync();
-    cudaError_t acquire(cudaStream_t stream, size_t n_counters, size_t n_flags);
+    cudaError_t acquire(cudaStream_t stream, size_t n_counters);
     cudaError_t release();
     int *counters = nullptr;
-    unsigned *flags = nullptr;
-    unsigned generation = 0;
 
    private:
     cudaStream_t stream_ = nullptr;
     void *owned_ = nullptr;              // captured launch: its block
     std::unique_lock<std::mutex> lock_;  // eager launch: the stream's entry
 };
-// Frees every stream's split counters and flags on the current device after
+// Frees every stream's split counters on the current device after
 // synchronising it (the next split call on a stream creates zeroed ones).
 // Used after a bounded wait ran out, when counters may be left mid-count.
 cudaError_t split_sync_release_device();
@@ -98,7 +93,7 @@ cudaError_t split_sync_release_device();
 // What the library holds on the current device between calls.
 struct MemoryInfo {
     uint64_t split_streams = 0;        // streams with split counters
-    uint64_t split_bytes = 0;          // bytes of those counters and flags
+    uint64_t split_bytes = 0;          // bytes of those counters
     uint64_t pool_used_bytes = 0;      // pool memory in use (counters, pending workspace)
     uint64_t pool_reserved_bytes = 0;  // pool memory held from the driver
 };

@@ -617,7 +617,7 @@ cudaError_t launch_cfg(const Problem &p, cudaStream_t stream, const char **name,
         } else {
             // partial sums from the pool; counters from the stream's split
             // counters (zero; the last contributor of a tile resets its own)
-            cudaError_t e = sync.acquire(stream, static_cast<size_t>(plan.tail_tiles), 0);
+            cudaError_t e = sync.acquire(stream, static_cast<size_t>(plan.tail_tiles));
             if (e != cudaSuccess) return e;
             args.ws_count = sync.counters;
             e = workspace_alloc(part_bytes, stream, &ws);

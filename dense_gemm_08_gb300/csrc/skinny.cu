@@ -480,7 +480,7 @@ cudaError_t launch_skinny(const Problem &p, InType in, cudaStream_t stream, cons
         } else {
             // partial sums from the pool; counters from the stream's split
             // counters (zero; the last slice of a column block resets its own)
-            cudaError_t e = sync.acquire(stream, static_cast<size_t>(a.n_cb), 0);
+            cudaError_t e = sync.acquire(stream, static_cast<size_t>(a.n_cb));
             if (e != cudaSuccess) return e;
             a.ws_count = sync.counters;
             e = workspace_alloc(part, stream, &ws);

@@ -12,9 +12,7 @@
 // kernel leaves the counters it used at zero when it completes (the last
 // piece of a tile resets its counter), so calls on a stream need no clearing
 // operation between them -- an extra stream operation between two GEMM
-// kernels keeps the second one from starting as the first drains.  Flags
-// that pieces wait on are compared with a per-stream generation number that
-// grows with every call, so they are never cleared either.
+// kernels keeps the second one from starting as the first drains.
 //
 // Streams are told apart by the stream's unique id (cudaStreamGetId), not
 // by the handle value: cudaStreamPerThread is one handle value for every
@@ -22,11 +20,9 @@
 // has two handle values (0 and cudaStreamLegacy).
 //
 // A call holds its stream's entry from SplitSync::acquire until the launch
-// is enqueued (SplitSync::release).  So, on one stream, launches are
-// enqueued in the order of the generation numbers they were given, and a
-// buffer that a stream outgrows is freed in stream order (cudaFreeAsync)
-// after every launch that was given it: any number of host threads may call
-// on one stream.
+// is enqueued (SplitSync::release).  So a buffer that a stream outgrows is
+// freed in stream order (cudaFreeAsync) after every launch that was given
+// it, and any number of host threads may call on one stream.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -102,9 +98,6 @@ struct SyncBuf {
     int dev = 0;
     int *counters = nullptr;
     size_t n_counters = 0;
-    unsigned *flags = nullptr;
-    size_t n_flags = 0;
-    unsigned generation = 0;
 };
 
 struct KeyHash {
@@ -157,38 +150,32 @@ cudaError_t release_device_locked(int dev) {
     for (auto &kv : g_sync) {
         SyncBuf &b = *kv.second;
         if (b.dev != dev) continue;
-        for (void *p : {static_cast<void *>(b.counters), static_cast<void *>(b.flags)}) {
-            if (p == nullptr) continue;
-            const cudaError_t ef = cudaFreeAsync(p, cudaStreamLegacy);
+        if (b.counters != nullptr) {
+            const cudaError_t ef = cudaFreeAsync(b.counters, cudaStreamLegacy);
             if (e == cudaSuccess) e = ef;
         }
         b.counters = nullptr;
-        b.flags = nullptr;
-        b.n_counters = b.n_flags = 0;
-        b.generation = 0;
+        b.n_counters = 0;
     }
     const cudaError_t es = cudaStreamSynchronize(cudaStreamLegacy);
     return e != cudaSuccess ? e : es;
 }
 }  // namespace
 
-cudaError_t SplitSync::acquire(cudaStream_t stream, size_t n_counters, size_t n_flags) {
+cudaError_t SplitSync::acquire(cudaStream_t stream, size_t n_counters) {
     stream_ = stream;
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(stream, &capture);
     if (e != cudaSuccess) return e;
     if (capture != cudaStreamCaptureStatusNone) {
-        // one zeroed block per captured launch: [counters][flags]
-        const size_t c_bytes = (n_counters * sizeof(int) + 15) & ~static_cast<size_t>(15);
-        size_t bytes = c_bytes + n_flags * sizeof(unsigned);
+        // one zeroed block of counters per captured launch
+        size_t bytes = n_counters * sizeof(int);
         if (bytes == 0) bytes = 16;
         void *blk = nullptr;
         if ((e = workspace_alloc(bytes, stream, &blk)) != cudaSuccess) return e;
         owned_ = blk;
         if ((e = cudaMemsetAsync(blk, 0, bytes, stream)) != cudaSuccess) return e;
         counters = static_cast<int *>(blk);
-        flags = reinterpret_cast<unsigned *>(static_cast<char *>(blk) + c_bytes);
-        generation = 1;
         return cudaSuccess;
     }
     int dev = 0;
@@ -207,18 +194,7 @@ cudaError_t SplitSync::acquire(cudaStream_t stream, size_t n_counters, size_t n_
     }
     lock_ = std::unique_lock<std::mutex>(b->m);
     if ((e = ensure(&b->counters, &b->n_counters, n_counters, stream)) != cudaSuccess) return e;
-    if ((e = ensure(&b->flags, &b->n_flags, n_flags, stream)) != cudaSuccess) return e;
-    if (++b->generation == 0) {
-        // after 2^32 calls on one stream: start the flags over from zero
-        if (b->n_flags > 0) {
-            e = cudaMemsetAsync(b->flags, 0, b->n_flags * sizeof(unsigned), stream);
-            if (e != cudaSuccess) return e;
-        }
-        b->generation = 1;
-    }
     counters = b->counters;
-    flags = b->flags;
-    generation = b->generation;
     return cudaSuccess;
 }
 
@@ -253,7 +229,7 @@ cudaError_t memory_info(MemoryInfo *out) {
             if (kv.first.first != dev) continue;
             std::lock_guard<std::mutex> entry_lock(kv.second->m);
             const SyncBuf &b = *kv.second;
-            const uint64_t bytes = b.n_counters * sizeof(int) + b.n_flags * sizeof(unsigned);
+            const uint64_t bytes = b.n_counters * sizeof(int);
             if (bytes == 0) continue;
             ++out->split_streams;
             out->split_bytes += bytes;

@@ -29,7 +29,10 @@
  *   keep every SM busy).  Such a kernel takes a temporary workspace for the
  *   partial sums (a few tens of MiB at most) from a memory pool the library
  *   owns, one per device, allocated and freed in stream order on `stream`.
- *   The pool keeps up to 256 MiB of freed memory for later calls.
+ *   The pool keeps up to 256 MiB of freed memory for later calls.  Kernels
+ *   that split a tile's K range over the CTAs of one thread-block cluster
+ *   (small tensor-core and FP32 problems) add the partial sums in the
+ *   cluster's shared memory and take neither workspace nor counters.
  *   Split counters: the split pieces count themselves in small counters that
  *   the library keeps per (device, stream) -- streams told apart by their
  *   unique id, so cudaStreamPerThread is a different stream in each host
@@ -48,9 +51,10 @@
  * Asynchrony: the work is enqueued on `stream` (0 = the legacy default
  *   stream) and the call returns without waiting for it.  The caller keeps
  *   the buffers alive until the stream has passed the call.
- * Shapes: M, N, K >= 0 and each <= 2^31 - 1.  M == 0 or N == 0 is a no-op
- *   that returns GEMM_OK without touching any pointer.  K == 0 or
- *   alpha == 0 gives D = beta * C (A and B are not read).
+ * Shapes: M, N, K >= 0 and each <= 2^31 - 1, and M * N <= 2^43 (no device
+ *   holds a larger D).  M == 0 or N == 0 is a no-op that returns GEMM_OK
+ *   without touching any pointer.  K == 0 or alpha == 0 gives
+ *   D = beta * C (A and B are not read).
  * beta == 0: C is never read and may be NULL (BLAS convention; C traffic
  *   only counts when beta != 0 in "GEMM on NVIDIA GPUs", section 2, "GEMM
  *   arithmetic intensity").  C == D with the same ldc/ldd is allowed

@@ -60,7 +60,9 @@ def test_argument_errors_without_a_device(fn_name):
     bad = [dict(M=-1), dict(N=-3), dict(K=-1), dict(M=1 << 31), dict(oa=2), dict(ocd=5),
            dict(lda=7), dict(ldb=7), dict(ldd=7), dict(oa=1, lda=7), dict(ocd=1, ldd=7),
            dict(beta=1.0), dict(beta=1.0, C=fake, ldc=7), dict(A=None), dict(B=None),
-           dict(D=None), dict(D=fake + 2), dict(A=fake + 1), dict(C=fake + 2, beta=1.0)]
+           dict(D=None), dict(D=fake + 2), dict(A=fake + 1), dict(C=fake + 2, beta=1.0),
+           # M * N above 2^43 (lda = K, ldb = ldd = N: leading dimensions valid)
+           dict(M=1 << 22, N=(1 << 21) + 1, ldb=(1 << 21) + 1, ldd=(1 << 21) + 1)]
     for change in bad:
         a = dict(good, **change)
         st = fn(a["M"], a["N"], a["K"], a["alpha"], a["A"], a["lda"], a["oa"], a["B"], a["ldb"],

@@ -95,7 +95,7 @@ def test_epilogue_every_path(variant, d_type):
     bias = bias_for(w, 34)
     expect = {"pair": "gemm_bf16_tc<pair,direct", "pair_staged": "gemm_bf16_tc<pair",
               "pair_tail": "gemm_bf16_tc<pair",
-              "splitk": "gemm_bf16_tc<splitk>",
+              "splitk": "gemm_bf16_tc<splitk,",
               "simt": "sgemm_simt<bf16", "scale_c": "scale_c", "col_major_d": "gemm_bf16_tc",
               "unaligned_d": "gemm_bf16_tc", "ragged_n": "gemm_bf16_tc"}[variant]
     # D rows on 32 bytes (the pair kernel's direct epilogue; TMA stores on the

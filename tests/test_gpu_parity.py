@@ -123,7 +123,7 @@ def test_tc_split_k_all_orders_full(orders):
     M, N, K = TC_SPLIT_SHAPE
     w = Workload("tc_splitk", M, N, K, 1.5, -0.25, "bf16", *orders)
     inp = make_inputs(w, seed=18, pad=3, ld_multiple=8)
-    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<splitk>")
+    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc<splitk,")
 
 
 def test_tc_split_k_deterministic_and_exact_on_integers():
@@ -131,7 +131,7 @@ def test_tc_split_k_deterministic_and_exact_on_integers():
     w = Workload("tc_splitk_int", M, N, K, 1.0, 0.0, "bf16", ROW, COL, ROW, dist="int")
     inp = make_inputs(w, seed=19)
     D1, _, name = run_gpu(w, inp)
-    assert name == "gemm_bf16_tc<splitk>"
+    assert name.startswith("gemm_bf16_tc<splitk,"), name
     ref, _ = oracle_full(w, inp)
     assert np.array_equal(logical_d(w, D1), ref.astype(np.float32))
     w = w.with_(dist="normal", alpha=0.5, beta=1.0)
@@ -141,9 +141,52 @@ def test_tc_split_k_deterministic_and_exact_on_integers():
     assert torch.equal(D1, D2)
 
 
+# The split-K cluster size ks is the largest of SMs // tiles, K blocks // 4
+# and 8 whose clusters (one per 128 x 256 tile) are all resident at once.
+# On 152 SMs these shapes ask for every size from 2 to 8 (fewer where a GPC
+# cannot hold that many clusters), with ragged M, N and K: warps whose rows
+# are all past M (M = 33), a last tile holding one partial 32-column chunk
+# (N = 520), a partial last K block, C and D through TMA boxes or row
+# copies.  (M, N, K, pad_d, beta)
+CLUSTER_SPLIT_SHAPES = [
+    (100, 200, 2048, 0, -0.25),    # 1 tile, 32 K blocks: 8 pieces
+    (33, 520, 4095, 3, 0.5),       # 3 tiles: 8 pieces, K blocks 64 (last partial)
+    (2432, 200, 2048, 0, 1.0),     # 19 tiles: 8 (or fewer, where 19 clusters of 8 do not fit)
+    (2688, 250, 1800, 3, -0.25),   # 21 tiles: 7
+    (3200, 256, 1536, 0, 0.0),     # 25 tiles: 6 (24 K blocks)
+    (3840, 230, 2000, 0, -0.25),   # 30 tiles: 5
+    (640, 1280, 999, 3, 1.0),      # 25 tiles, 16 K blocks: 4
+    (1200, 1200, 2000, 0, -0.25),  # 50 tiles: 3
+    (1000, 1000, 640, 3, 0.0),     # 32 tiles, 10 K blocks: 2
+    (300, 600, 200, 0, -0.25),     # 4 K blocks: no split
+]
+
+
+@pytest.mark.parametrize("shape", CLUSTER_SPLIT_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k, _, _ in
+                                                            CLUSTER_SPLIT_SHAPES])
+def test_tc_cluster_split_sizes_full(shape):
+    M, N, K, pad_d, beta = shape
+    w = Workload("tc_cluster", M, N, K, 1.5, beta, "bf16", ROW, COL, ROW)
+    inp = make_inputs(w, seed=M + N + K, ld_multiple=8)
+    D, ref, _ = full_check(w, inp, pad_d=pad_d, expect_kernel="gemm_bf16_tc")
+    name = lib.gemm_last_kernel()
+    tiles = -(-M // 128) * -(-N // 256)
+    want_max = min(torch.cuda.get_device_properties(0).multi_processor_count // tiles,
+                   -(-K // 64) // 4, 8)
+    if want_max < 2:
+        assert name == "gemm_bf16_tc", name
+    else:
+        assert name.startswith("gemm_bf16_tc<splitk,x"), name
+        ks = int(name[len("gemm_bf16_tc<splitk,x"):-1])
+        assert 2 <= ks <= want_max, name
+        # the pieces are added in K order: a second call gives the same bits
+        D2, _, _ = run_gpu(w, inp, pad_d=pad_d)
+        assert np.array_equal(logical_d(w, D2), D)
+
+
 @pytest.mark.parametrize("orders", [(ROW, COL, ROW), (COL, ROW, COL)])
 def test_f16_pair_and_split_variants_full(orders):
-    for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk>")]:
+    for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk,")]:
         M, N, K = shape
         w = Workload("f16var", M, N, K, 1.5, -0.25, "f16", *orders)
         inp = make_inputs(w, seed=22, pad=5, ld_multiple=8)

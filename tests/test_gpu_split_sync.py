@@ -1,14 +1,16 @@
 """GPU tests of the split kernels' per-stream counters.
 
-Every kernel that splits a tile's K range (tensor-core split-K, the CTA-pair
-kernel's split last round, the CUDA-core stream-K tail, the small-M kernel's
-K slices) counts the finished pieces in counters that belong to the stream
-and persist between calls; the piece that completes a count returns it to
-zero, so no call clears them (a captured call takes fresh zeroed counters
-instead).  These tests check that calls of every variant -- back to back in
-any order, on two streams at once, after a kernel gave up a bounded wait, and
-replayed from a captured graph beside eager calls -- give the same bits as a
-first call that is checked against the oracle.  Calls may come from any
+Kernels that split a tile's K range over CTAs that are not one cluster (the
+CTA-pair kernel's split last round, the CUDA-core stream-K tail, the small-M
+kernel's K slices) count the finished pieces in counters that belong to the
+stream and persist between calls; the piece that completes a count returns
+it to zero, so no call clears them (a captured call takes fresh zeroed
+counters instead).  The single-CTA tensor-core split-K adds its pieces
+inside a thread-block cluster and takes no counters; it runs beside the
+others here.  These tests check that calls of every variant -- back to back
+in any order, on two streams at once, after a kernel gave up a bounded wait,
+and replayed from a captured graph beside eager calls -- give the same bits
+as a first call that is checked against the oracle.  Calls may come from any
 number of host threads, on one stream or on several (cudaStreamPerThread
 included); counters a stream outgrows are freed in stream order."""
 import numpy as np
@@ -23,9 +25,9 @@ pytestmark = pytest.mark.gpu
 
 # (workload, expected kernel prefix)
 CASES = [
-    (Workload("tc_splitk", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW), "gemm_bf16_tc<splitk>"),
+    (Workload("tc_splitk", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW), "gemm_bf16_tc<splitk,"),
     (Workload("pair_tail", 2304, 2560, 1024, 0.5, 1.0, "bf16", ROW, COL, ROW), "gemm_bf16_tc<pair"),
-    (Workload("f16_splitk", 300, 600, 2048, 1.0, 0.5, "f16", COL, ROW, COL), "gemm_f16_tc<splitk>"),
+    (Workload("f16_splitk", 300, 600, 2048, 1.0, 0.5, "f16", COL, ROW, COL), "gemm_f16_tc<splitk,"),
     (Workload("simt_splitk", 384, 384, 1000, 1.5, -0.25, "f32", ROW, ROW, ROW), "sgemm_simt<f32"),
     (Workload("simt_tail", 2560, 2048, 512, 1.0, 0.0, "f32", ROW, COL, ROW), "sgemm_simt<f32"),
     (Workload("skinny", 4, 3000, 5000, 1.5, -0.25, "f32", ROW, ROW, ROW), "skinny<f32"),
@@ -259,38 +261,62 @@ def test_per_thread_default_stream_in_two_threads(cases):
 
 
 def test_outgrown_counters_are_freed():
-    """Ten calls on one stream, each splitting more tiles than the last, grow
-    the stream's counters ten times; each outgrown buffer is freed in stream
-    order, so afterwards the stream holds one buffer (the last size) and the
-    pool has nothing else in use.  gemm_release_memory frees even that, and
-    the next call starts from fresh counters.  Every result is checked
-    against the oracle."""
+    """Eleven calls on one stream, each splitting more column blocks than the
+    last, grow the stream's counters ten times; each outgrown buffer is freed
+    in stream order, so afterwards the stream holds one buffer (the last
+    size) and the pool has nothing else in use.  gemm_release_memory frees
+    even that, and the next call starts from fresh counters.  Every result is
+    checked against the oracle."""
     lib.gemm_release_memory()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     sizes = []
-    # 128 x 256 tiles, one column of them: t tiles split K (t < 76 on GB300),
-    # each with 4 counters and 4 flags
-    for t in (1, 5, 9, 13, 17, 21, 25, 29, 33, 37, 41):
-        w = Workload(f"grow_{t}", 128 * t, 256, 1024, 1.0, 0.0, "bf16", ROW, COL, ROW)
-        c = Case(w, "gemm_bf16_tc<splitk>", seed=t)
+    # the small-M kernel on row-major B: one counter per 128-column block,
+    # t blocks (K = 2048 is cut into at least two slices for every t here)
+    for t in (1, 17, 33, 49, 65, 81, 97, 113, 129, 145, 161):
+        w = Workload(f"grow_{t}", 4, 128 * t, 2048, 1.0, 0.0, "f32", ROW, ROW, ROW)
+        c = Case(w, "skinny<f32", seed=t)
         D = c.launch(s)
         s.synchronize()
         c.check_against_oracle(D)
         info = lib.gemm_memory_info()
         assert info["split_streams"] == 1, info
         sizes.append(info["split_bytes"])
-        assert info["pool_used_bytes"] == info["split_bytes"], info
     assert all(b > a for a, b in zip(sizes, sizes[1:])), sizes  # ten growths
-    # counters + flags of the last call only, each 164 words rounded up to 16
-    assert sizes[-1] == 2 * 176 * 4, sizes
+    # the last call's 161 counters, rounded up to 16 words
+    assert sizes[-1] == 176 * 4, sizes
     assert lib.gemm_release_memory() == lib.GEMM_OK
     info = lib.gemm_memory_info()
     assert info["split_streams"] == 0 and info["split_bytes"] == 0, info
     assert info["pool_used_bytes"] == 0 and info["pool_reserved_bytes"] == 0, info
-    w = Workload("after_release", 300, 600, 2048, 1.5, -0.25, "bf16", ROW, COL, ROW)
-    c = Case(w, "gemm_bf16_tc<splitk>", seed=99)
+    w = Workload("after_release", 4, 3000, 5000, 1.5, -0.25, "f32", ROW, ROW, ROW)
+    c = Case(w, "skinny<f32", seed=99)
     D = c.launch(s)
     s.synchronize()
     c.check_against_oracle(D)
+    assert lib.gemm_last_device_status() == lib.GEMM_OK
+
+
+def test_cluster_split_takes_no_memory():
+    """The single-CTA tensor-core split-K adds its K pieces in the shared
+    memory of one thread-block cluster: calls of it, eager and captured,
+    leave the library's pool and the stream's counters untouched."""
+    assert lib.gemm_release_memory() == lib.GEMM_OK
+    cases = [Case(w, prefix, seed=60 + i) for i, (w, prefix) in enumerate(CASES)
+             if prefix.startswith("gemm_") and "splitk" in prefix]
+    assert len(cases) == 2
+    first = [c.launch() for c in cases]
+    torch.cuda.synchronize()
+    for c, D in zip(cases, first):
+        c.check_against_oracle(D)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = [c.launch() for c in cases]
+    graph.replay()
+    torch.cuda.synchronize()
+    for D, ref in zip(captured, first):
+        assert torch.equal(D, ref)
+    info = lib.gemm_memory_info()
+    assert info["split_streams"] == 0 and info["split_bytes"] == 0, info
+    assert info["pool_used_bytes"] == 0 and info["pool_reserved_bytes"] == 0, info
     assert lib.gemm_last_device_status() == lib.GEMM_OK
