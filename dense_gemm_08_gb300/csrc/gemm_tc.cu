@@ -576,12 +576,16 @@ __device__ __forceinline__ void box_store_rows(const uint8_t *box, const TcArgs 
                                                int64_t c0, int lane) {
     const int64_t col = c0 + lane;
     const bool col_ok = col < a.N;
+    // all 32 box reads first: a read placed after a store to D could not be
+    // started before it (the compiler cannot tell the two pointers apart),
+    // which would make every row wait out a shared-memory round trip
+    float d[32];
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-        const int64_t r = row0 + rr;
-        const float d = *reinterpret_cast<const float *>(box + box_offset(rr, lane));
-        if (col_ok && r < a.M) a.D[r * a.ldd + col] = d;
-    }
+    for (int rr = 0; rr < 32; ++rr) d[rr] = *reinterpret_cast<const float *>(box + box_offset(rr, lane));
+    float *dp = a.D + row0 * a.ldd + col;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+        if (col_ok && row0 + rr < a.M) dp[rr * a.ldd] = d[rr];
 }
 
 // BF16 box (32 rows of 64 bytes, unswizzled) into D[row0 + rr, c0 + lane],
@@ -590,13 +594,13 @@ __device__ __forceinline__ void box_store_rows_bf16(const uint8_t *box, const Tc
                                                     int64_t row0, int64_t c0, int lane) {
     const int64_t col = c0 + lane;
     const bool col_ok = col < a.N;
-    uint16_t *d16 = reinterpret_cast<uint16_t *>(a.D);
+    uint16_t d[32];  // all box reads before the first store, as in box_store_rows
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-        const int64_t r = row0 + rr;
-        const uint16_t d = *reinterpret_cast<const uint16_t *>(box + rr * 64 + lane * 2);
-        if (col_ok && r < a.M) d16[r * a.ldd + col] = d;
-    }
+    for (int rr = 0; rr < 32; ++rr) d[rr] = *reinterpret_cast<const uint16_t *>(box + rr * 64 + lane * 2);
+    uint16_t *dp = reinterpret_cast<uint16_t *>(a.D) + row0 * a.ldd + col;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+        if (col_ok && row0 + rr < a.M) dp[rr * a.ldd] = d[rr];
 }
 
 // 32 bytes (eight 32-bit words) to global memory in one store.
@@ -1460,6 +1464,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 };
                 cluster_sync();  // (A)
                 ++cluster_bars;
+                // rows past M are never stored to D: they are not sent (and
+                // their slots are read but unused)
+                const bool row_ok = row0 + lane < args.M;
 #pragma unroll 1
                 for (int chunk = 0; chunk < n_chunks; ++chunk) {
                     const int owner = chunk % ks;
@@ -1472,10 +1479,12 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     const uint32_t dst_local = ring_base + static_cast<uint32_t>(
                         ((quarter * own_max + chunk / ks) * (ks - 1) + idx) * 4096);
                     const uint32_t dst = map_to_rank(dst_local, static_cast<uint32_t>(owner));
+                    if (row_ok) {
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4)
-                        st_cluster_v4(dst + slot_offset(lane, j4), v[j4 * 4 + 0], v[j4 * 4 + 1],
-                                      v[j4 * 4 + 2], v[j4 * 4 + 3]);
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            st_cluster_v4(dst + slot_offset(lane, j4), v[j4 * 4 + 0],
+                                          v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
+                    }
                 }
                 cluster_sync();  // (C)
                 ++cluster_bars;
