@@ -544,22 +544,32 @@ __device__ __forceinline__ uint32_t slot_offset(int r, int j4) {
     return static_cast<uint32_t>(j4 * 512 + r * 16);
 }
 
+// Rows of the 32-row block at row0 that lie inside the matrix (0 to 32).
+__device__ __forceinline__ int rows_inside(const TcArgs &a, int64_t row0) {
+    const int64_t left = a.M - row0;
+    return left <= 0 ? 0 : (left >= 32 ? 32 : static_cast<int>(left));
+}
+
 // Start copying C[row0 + rr, c0 + lane], rr < 32, into the box with 4-byte
 // asynchronous copies (one coalesced row per instruction; elements outside
 // the matrix are zero-filled) and commit them as one group of this thread.
+// The row pointer advances by ldc and the box address is fixed per row, so
+// a row costs a handful of instructions.
 __device__ __forceinline__ void box_load_rows_async(uint8_t *box, const TcArgs &a, int64_t row0,
                                                     int64_t c0, int lane) {
-    const int64_t col = c0 + lane;
-    const bool col_ok = col < a.N;
+    const int nrows = rows_inside(a, row0);
+    const bool col_ok = c0 + lane < a.N;
+    const float *src = a.C + (nrows > 0 ? row0 * a.ldc + c0 + lane : 0);
+    const uint32_t dst = smem_addr(box) + static_cast<uint32_t>((lane & 3) * 4);
+    const uint32_t quad = static_cast<uint32_t>(lane >> 2);
 #pragma unroll
     for (int rr = 0; rr < 32; ++rr) {
-        const int64_t r = row0 + rr;
-        const bool ok = col_ok && r < a.M;
-        const float *src = ok ? a.C + r * a.ldc + col : a.C;
+        const bool ok = col_ok && rr < nrows;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                         smem_addr(box + box_offset(rr, lane))),
-                     "l"(src), "r"(ok ? 4 : 0)
+                         dst + static_cast<uint32_t>(rr * 128) + ((quad ^ (rr & 7)) << 4)),
+                     "l"(ok ? src : a.C), "r"(ok ? 4 : 0)
                      : "memory");
+        src += a.ldc;
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -574,33 +584,37 @@ __device__ __forceinline__ void async_copy_wait() {
 // to the matrix.
 __device__ __forceinline__ void box_store_rows(const uint8_t *box, const TcArgs &a, int64_t row0,
                                                int64_t c0, int lane) {
-    const int64_t col = c0 + lane;
-    const bool col_ok = col < a.N;
+    const int nrows = rows_inside(a, row0);
+    const bool col_ok = c0 + lane < a.N;
     // all 32 box reads first: a read placed after a store to D could not be
     // started before it (the compiler cannot tell the two pointers apart),
     // which would make every row wait out a shared-memory round trip
     float d[32];
 #pragma unroll
     for (int rr = 0; rr < 32; ++rr) d[rr] = *reinterpret_cast<const float *>(box + box_offset(rr, lane));
-    float *dp = a.D + row0 * a.ldd + col;
+    float *dp = a.D + (nrows > 0 ? row0 * a.ldd + c0 + lane : 0);
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr)
-        if (col_ok && row0 + rr < a.M) dp[rr * a.ldd] = d[rr];
+    for (int rr = 0; rr < 32; ++rr) {
+        if (col_ok && rr < nrows) *dp = d[rr];
+        dp += a.ldd;
+    }
 }
 
 // BF16 box (32 rows of 64 bytes, unswizzled) into D[row0 + rr, c0 + lane],
 // one coalesced row per step, clipped to the matrix.
 __device__ __forceinline__ void box_store_rows_bf16(const uint8_t *box, const TcArgs &a,
                                                     int64_t row0, int64_t c0, int lane) {
-    const int64_t col = c0 + lane;
-    const bool col_ok = col < a.N;
+    const int nrows = rows_inside(a, row0);
+    const bool col_ok = c0 + lane < a.N;
     uint16_t d[32];  // all box reads before the first store, as in box_store_rows
 #pragma unroll
     for (int rr = 0; rr < 32; ++rr) d[rr] = *reinterpret_cast<const uint16_t *>(box + rr * 64 + lane * 2);
-    uint16_t *dp = reinterpret_cast<uint16_t *>(a.D) + row0 * a.ldd + col;
+    uint16_t *dp = reinterpret_cast<uint16_t *>(a.D) + (nrows > 0 ? row0 * a.ldd + c0 + lane : 0);
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr)
-        if (col_ok && row0 + rr < a.M) dp[rr * a.ldd] = d[rr];
+    for (int rr = 0; rr < 32; ++rr) {
+        if (col_ok && rr < nrows) *dp = d[rr];
+        dp += a.ldd;
+    }
 }
 
 // 32 bytes (eight 32-bit words) to global memory in one store.
