@@ -819,7 +819,7 @@ def bench_sweep_stages(args):
     _build.build()
     with ThreadPoolExecutor(len(stages)) as ex:
         paths = list(ex.map(lambda S: _build.build_variant(
-            f"stages{S}", {"GEMM_TC_DIRECT_STAGES": S, "GEMM_TC_PAIR_STAGES": min(S, 6)}),
+            f"stages{S}", {"GEMM_TC_DIRECT_STAGES": S, "GEMM_TC_PAIR_STAGES": min(S, 5)}),
             stages))
     libs = dict(zip(stages, paths))
     runs = {"bf16_8192": {S: [] for S in stages}, "bf16_mlp": {S: [] for S in stages}}

@@ -59,18 +59,18 @@ constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512: all of TMEM
 constexpr int kGroupM = 16;               // grouped raster width (tile rows)
 
 // Depth of the CTA pair's operand ring (stages of 32 KiB per CTA).  With the
-// epilogue's staging boxes six stages fit; without them (the direct
-// epilogue, below) seven.  A build may set fewer (-DGEMM_TC_PAIR_STAGES=S,
-// 2 <= S <= 6; -DGEMM_TC_DIRECT_STAGES=S, 2 <= S <= 7) to measure
-// throughput against depth.
+// epilogue's staging boxes (64 KiB) five stages fit; without them (the
+// direct epilogue, below) seven.  A build may set fewer
+// (-DGEMM_TC_PAIR_STAGES=S, 2 <= S <= 5; -DGEMM_TC_DIRECT_STAGES=S,
+// 2 <= S <= 7) to measure throughput against depth.
 #ifndef GEMM_TC_PAIR_STAGES
-#define GEMM_TC_PAIR_STAGES 6
+#define GEMM_TC_PAIR_STAGES 5
 #endif
 #ifndef GEMM_TC_DIRECT_STAGES
 #define GEMM_TC_DIRECT_STAGES 7
 #endif
-static_assert(GEMM_TC_PAIR_STAGES >= 2 && GEMM_TC_PAIR_STAGES <= 6,
-              "the staged pair ring holds 2 to 6 stages");
+static_assert(GEMM_TC_PAIR_STAGES >= 2 && GEMM_TC_PAIR_STAGES <= 5,
+              "the staged pair ring holds 2 to 5 stages");
 static_assert(GEMM_TC_DIRECT_STAGES >= 2 && GEMM_TC_DIRECT_STAGES <= 7,
               "the direct pair ring holds 2 to 7 stages");
 
@@ -89,11 +89,12 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES =
         CG == 1 ? 4 : (DIRECT ? GEMM_TC_DIRECT_STAGES : GEMM_TC_PAIR_STAGES);
-    // epilogue warps: eight (two per TMEM lane quarter, one 32 x 32 FP32 box
-    // of 4 KiB each) for the staged CTA pair, whose epilogue is its limit
-    // when K is short; four (two boxes each) otherwise
+    // epilogue warps: eight (two per TMEM lane quarter) for the staged CTA
+    // pair, whose epilogue is its limit when K is short; four otherwise.
+    // Each has two 32 x 32 FP32 boxes of 4 KiB (C for the next chunk
+    // arrives in one while the other is in use).
     static constexpr int EPI_WARPS = (CG == 2 && !DIRECT) ? 8 : 4;
-    static constexpr int BOXES = EPI_WARPS == 8 ? 1 : 2;
+    static constexpr int BOXES = 2;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int STAGING_BYTES = DIRECT ? 0 : EPI_WARPS * BOXES * 32 * 32 * 4;
     // ring + staging + barriers + slack for aligning the ring to 1024 bytes
@@ -792,8 +793,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
     uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
     uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
-    uint64_t *cbar = drain + 1;              // [8]       C box loaded (epilogue warp x box)
-    uint64_t *pbar = cbar + 8;               // [8]       split-K pieces loaded (epilogue warp)
+    uint64_t *cbar = drain + 1;              // [16]      C box loaded (epilogue warp x box)
+    uint64_t *pbar = cbar + 16;              // [8]       split-K pieces loaded (epilogue warp)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pbar + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -815,7 +816,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             mbar_init(smem_addr(&tempty[b]), C::EPI_WARPS * CG);
         }
         mbar_init(smem_addr(drain), 1);
-        for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&cbar[i]), 1);
+        for (int i = 0; i < 16; ++i) mbar_init(smem_addr(&cbar[i]), 1);
         for (int i = 0; i < 8; ++i) mbar_init(smem_addr(&pbar[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1168,52 +1169,63 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
         __syncwarp();
     } else if constexpr (C::EPI_WARPS == 8) {
         // -------------------------------------- epilogue warps 2-9, staged, wide
-        // Two warps per TMEM lane quarter (warp % 4), one box each: warp
+        // Two warps per TMEM lane quarter (warp % 4), two boxes each: warp
         // e = warp - 2 drains the chunks of parity e / 4 of its quarter's 32
         // accumulator rows, so two chunks of a quarter are in flight at once.
-        // Per chunk: C into the box (TMA, or coalesced row loads) -> tcgen05.ld
-        // -> D = alpha * acc + beta * C in registers -> the box -> one TMA
-        // store (or coalesced row stores when D's pitch cannot be described to
-        // TMA).
+        // Per chunk: C into a box (TMA, or coalesced row loads), started
+        // while the previous chunk is processed -> tcgen05.ld -> D = alpha *
+        // acc + beta * C in registers -> the box -> one TMA store (or
+        // coalesced row stores when D's pitch cannot be described to TMA).
         const int e = warp - 2;
         const int quarter = warp % 4;  // TMEM lanes this warp may access
         const int half = e / 4;        // this warp's chunks: half, half + 2, ...
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool use_c = args.beta != 0.f;
         const bool tma_c = use_c && args.tma_c;
-        uint8_t *box = staging + e * 4096;
-        const uint32_t cb = smem_addr(&cbar[e]);
+        uint8_t *const boxes = staging + e * 2 * 4096;  // this warp's two boxes
+        uint8_t *box = boxes;                            // the box in use
+        const uint32_t cb0 = smem_addr(&cbar[e * 2]);
         const uint32_t pb = smem_addr(&pbar[e]);
-        uint32_t cphase = 0;  // parity of the box's next C arrival
+        uint32_t cphase = 0;  // bit b: parity of box b's next C arrival
         uint32_t pphase = 0;  // parity of the next split-K piece batch
         bool stop = false;
         auto emit_chunk = [&](float (&o)[32], int64_t r0, int64_t c0) {
             emit_box_chunk(o, box, r0, c0, lane, args, &map_d);
         };
-        auto box_free = [&]() {  // no TMA store still reads the box
-            if (lane == 0) bulk_wait_read<0>();
+        // at most the `pending` most recent TMA stores of D (one per chunk,
+        // issued in chunk order) may still be reading their boxes
+        auto box_free = [&](int pending) {
+            if (lane == 0) {
+                if (pending) bulk_wait_read<1>();
+                else bulk_wait_read<0>();
+            }
             __syncwarp();
         };
-        auto load_c = [&](int64_t c0, int64_t r0) {  // the box is free
+        auto load_c = [&](int b, int64_t c0, int64_t r0) {  // box b is free
             if (tma_c) {
                 if (lane == 0) {
+                    const uint32_t cb = cb0 + 8 * b;
                     mbar_arrive_expect_tx(cb, 32 * 32 * 4);
-                    tma_load_2d<CG>(smem_addr(box), &map_c, static_cast<int32_t>(c0),
+                    tma_load_2d<CG>(smem_addr(boxes + b * 4096), &map_c, static_cast<int32_t>(c0),
                                     static_cast<int32_t>(r0), map_to_rank(cb, rank));
                 }
             } else {
-                box_load_rows_async(box, args, r0, c0, lane);
+                box_load_rows_async(boxes + b * 4096, args, r0, c0, lane);
             }
         };
-        auto wait_c = [&]() -> bool {
+        // C of box b has landed (`later`: one more load was started after it)
+        auto wait_c = [&](int b, bool later) -> bool {
             if (tma_c) {
                 int landed = 1;
-                if (lane == 0) landed = wait_bounded(cb, cphase, abort_flag, args.timeout_ns);
+                if (lane == 0)
+                    landed = wait_bounded(cb0 + 8 * b, (cphase >> b) & 1u, abort_flag,
+                                          args.timeout_ns);
                 landed = __shfl_sync(0xffffffffu, landed, 0);
-                cphase ^= 1u;
+                cphase ^= 1u << b;
                 return landed != 0;
             }
-            async_copy_wait<0>();
+            if (later) async_copy_wait<1>();
+            else async_copy_wait<0>();
             __syncwarp();
             return true;
         };
@@ -1280,7 +1292,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     uint32_t v[32];
                     __syncwarp();
                     tmem_load_32cols(t_acc + chunk * 32, v);
-                    box_free();
+                    box_free(0);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4)
                         *reinterpret_cast<uint4 *>(box + box_offset(lane, j4 * 4)) =
@@ -1309,14 +1321,14 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
 #pragma unroll 1
                 for (int chunk = half; chunk < n_chunks && !stop; chunk += 2) {
                     const int64_t c0 = col0 + chunk * 32;
-                    box_free();
+                    box_free(0);
                     if (lane == 0) {
                         mbar_arrive_expect_tx(pb, static_cast<uint32_t>(it.nsp) * 4096);
                         for (int s2 = 0; s2 < it.nsp; ++s2)
                             bulk_copy_to_shared(smem_addr(pieces + s2 * 4096), piece_box(s2, chunk),
                                                 4096, pb);
                     }
-                    if (use_c) load_c(c0, row0);
+                    if (use_c) load_c(0, c0, row0);
                     int got = 1;
                     if (lane == 0) got = wait_bounded(pb, pphase, abort_flag, args.timeout_ns);
                     got = __shfl_sync(0xffffffffu, got, 0);
@@ -1345,7 +1357,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] *= args.alpha;
                     if (use_c) {
-                        if (!wait_c()) {
+                        if (!wait_c(0, false)) {
                             if (lane == 0) raise_abort(abort_flag);
                             aborted = stop = true;
                             break;
@@ -1357,11 +1369,24 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 }
                 continue;
             }
+            // chunk k of this warp (chunk half + 2k) uses box k & 1; C of the
+            // next chunk is started before this one is processed
+            if (my_last >= 0) {
+                box_free(0);  // every store of the previous tile has read its box
+                if (use_c) load_c(0, col0 + half * 32, row0);
+            }
 #pragma unroll 1
-            for (int chunk = half; chunk < n_chunks; chunk += 2) {
+            for (int chunk = half, k = 0; chunk < n_chunks; chunk += 2, ++k) {
                 const int64_t c0 = col0 + chunk * 32;
-                box_free();
-                if (use_c) load_c(c0, row0);
+                const int b = k & 1;
+                box = boxes + b * 4096;
+                const bool next = chunk + 2 < n_chunks;
+                if (use_c && next) {
+                    box_free(0);  // the store of chunk k - 1 has read box b ^ 1
+                    load_c(b ^ 1, c0 + 64, row0);
+                } else if (!use_c && k >= 2) {
+                    box_free(1);  // the store of chunk k - 2 has read box b
+                }
                 uint32_t v[32];
                 __syncwarp();  // tcgen05.ld is warp-collective: converge first
                 tmem_load_32cols(t_acc + chunk * 32, v);
@@ -1370,7 +1395,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) o[j] = args.alpha * __uint_as_float(v[j]);
                 if (use_c) {
-                    if (!wait_c()) {
+                    if (!wait_c(b, next)) {
                         if (lane == 0) raise_abort(abort_flag);
                         aborted = stop = true;
                         break;
@@ -1379,6 +1404,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 }
                 emit_chunk(o, row0, c0);
             }
+            box = boxes;
             if (my_last < 0) release_acc();
         }
         if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
