@@ -89,6 +89,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES =
         CG == 1 ? 4 : (DIRECT ? GEMM_TC_DIRECT_STAGES : GEMM_TC_PAIR_STAGES);
+    // single CTAs with a narrow B tile (N <= 128: 64 or 128 rows of B per
+    // stage) cut the same ring into more, smaller stages, at most 8
+    static constexpr int MAX_STAGES = CG == 1 ? 8 : STAGES;
     // epilogue warps: eight (two per TMEM lane quarter) for the staged CTA
     // pair, whose epilogue is its limit when K is short; four otherwise.
     // Each has two 32 x 32 FP32 boxes of 4 KiB (C for the next chunk
@@ -152,6 +155,11 @@ struct TcArgs {
     // (cluster rank = piece), which add their partial sums through
     // distributed shared memory (no workspace)
     int cluster_k;
+    // CG = 1: columns of B per tile (BN, or 64 / 128 when N fits: one tile
+    // column, a narrower B box and N = bn1 MMAs) and the ring cut to match
+    int bn1;
+    int stages1;
+    uint32_t stage_bytes1;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -491,7 +499,7 @@ __device__ __forceinline__ WorkItem work_item(int64_t w, const TcArgs &a) {
         it.nsp = a.tail_ks;
     }
     it.n_off = 0;
-    it.n_width = BN;
+    it.n_width = CG == 1 ? a.bn1 : BN;
     if (CG == 2 && a.tail_split_n && w >= a.tail_first) {
         // an N half of a tail tile, whole K
         it.n_off = it.sp * (BN / 2);
@@ -788,9 +796,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     uint8_t *ring = smem;
     uint8_t *staging = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned epilogue boxes
     uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING_BYTES);
-    uint64_t *full = bars;                   // [STAGES]  TMA -> MMA (leader counts both CTAs)
-    uint64_t *empty = bars + C::STAGES;      // [STAGES]  MMA -> TMA
-    uint64_t *tfull = bars + 2 * C::STAGES;  // [2]       MMA -> epilogue
+    uint64_t *full = bars;                       // [MAX_STAGES]  TMA -> MMA (leader counts both CTAs)
+    uint64_t *empty = bars + C::MAX_STAGES;      // [MAX_STAGES]  MMA -> TMA
+    uint64_t *tfull = bars + 2 * C::MAX_STAGES;  // [2]           MMA -> epilogue
     uint64_t *tempty = tfull + ACC_BUFS;     // [2]       epilogue -> MMA (leader counts both)
     uint64_t *drain = tempty + ACC_BUFS;     // [1]       MMA teardown
     uint64_t *cbar = drain + 1;              // [16]      C box loaded (epilogue warp x box)
@@ -806,7 +814,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     const int64_t num_groups = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::MAX_STAGES; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
         }
@@ -848,6 +856,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
 
     const int64_t n_items = work_items<CG>(args);
     const uint32_t ring_base = smem_addr(ring);
+    // ring stages (compile-time for CTA pairs)
+    const int stages = CG == 1 ? args.stages1 : C::STAGES;
+    const uint32_t stage_bytes = CG == 1 ? args.stage_bytes1 : C::STAGE_BYTES;
     bool aborted = false;
 
     if (warp == 0) {
@@ -884,7 +895,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     const uint32_t fb_local = smem_addr(&full[stage]);
                     // the leader's full barrier counts both CTAs' bytes
                     const uint32_t fb = CG == 1 ? fb_local : map_to_rank(fb_local, 0);
-                    const uint32_t sa = ring_base + stage * C::STAGE_BYTES;
+                    const uint32_t sa = ring_base + stage * stage_bytes;
                     const uint32_t sb = sa + C::A_BYTES;
                     const int32_t k0 = static_cast<int32_t>(kb * BK);
                     if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
@@ -895,13 +906,15 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                             tma_load_2d<CG>(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
                     }
                     if (args.b_kmajor) {
-                        tma_load_2d<CG>(sb, b_rows == C::B_ROWS ? &map_b : &map_b_half, k0, n0, fb);
+                        // (single CTAs: map_b's box is bn1 rows, the item's width)
+                        tma_load_2d<CG>(sb, (CG == 1 || b_rows == C::B_ROWS) ? &map_b : &map_b_half,
+                                        k0, n0, fb);
                     } else {
                         for (int i = 0; i < b_rows / 64; ++i)
                             tma_load_2d<CG>(sb + i * 64 * 128, &map_b, n0 + 64 * i, k0, fb);
                     }
                     ++issued;
-                    if (++stage == C::STAGES) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -912,12 +925,12 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             // CG = 2: the leader's full barriers also count the peer's bytes,
             // so the leader's drain covers both CTAs' copies.
             if (leader) {
-                const int64_t outstanding = issued < C::STAGES ? issued : C::STAGES;
+                const int64_t outstanding = issued < stages ? issued : stages;
                 int s = stage;
                 uint32_t ph = phase;
                 for (int64_t i = 0; i < outstanding; ++i) {
                     if (--s < 0) {
-                        s = C::STAGES - 1;
+                        s = stages - 1;
                         ph ^= 1;
                     }
                     const volatile int never = 0;  // issued copies complete regardless of aborts
@@ -939,6 +952,9 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 make_idesc(C::TILE_M, BN, !args.a_kmajor, !args.b_kmajor, args.ab_format);
             const uint32_t idesc_half =
                 make_idesc(C::TILE_M, BN / 2, !args.a_kmajor, !args.b_kmajor, args.ab_format);
+            const uint32_t idesc_n1 =  // single CTAs: N = bn1
+                make_idesc(C::TILE_M, CG == 1 ? args.bn1 : BN, !args.a_kmajor, !args.b_kmajor,
+                           args.ab_format);
             int stage = 0;
             uint32_t phase = 0;
             int64_t li = 0;
@@ -961,7 +977,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 const int64_t kb_end = it.kb_end;
                 const int buf = static_cast<int>(li & 1);
                 const uint32_t acc_phase = static_cast<uint32_t>((li >> 1) & 1);
-                const uint32_t idesc = it.n_width == BN ? idesc_full : idesc_half;
+                const uint32_t idesc =
+                    CG == 1 ? idesc_n1 : (it.n_width == BN ? idesc_full : idesc_half);
                 if (!wait_bounded(smem_addr(&tempty[buf]), acc_phase ^ 1, abort_flag,
                                   args.timeout_ns)) {
                     raise_abort(abort_flag);
@@ -976,7 +993,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     const bool two = i + 1 < nkb;
                     const int s0 = stage;
                     const uint32_t p0 = phase;
-                    const int s1 = s0 + 1 == C::STAGES ? 0 : s0 + 1;
+                    const int s1 = s0 + 1 == stages ? 0 : s0 + 1;
                     const uint32_t p1 = s1 == 0 ? p0 ^ 1u : p0;
                     const uint32_t fb0 = full0 + 8u * static_cast<uint32_t>(s0);
                     const uint32_t fb1 = full0 + 8u * static_cast<uint32_t>(s1);
@@ -992,15 +1009,15 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    uint64_t ad = a_desc0 + static_cast<uint64_t>(s0) * (C::STAGE_BYTES >> 4);
-                    uint64_t bd = b_desc0 + static_cast<uint64_t>(s0) * (C::STAGE_BYTES >> 4);
+                    uint64_t ad = a_desc0 + static_cast<uint64_t>(s0) * (stage_bytes >> 4);
+                    uint64_t bd = b_desc0 + static_cast<uint64_t>(s0) * (stage_bytes >> 4);
                     tc_mma<CG>(d_tmem, ad, bd, idesc, i > 0 ? 1u : 0u);
                     tc_mma<CG>(d_tmem, ad + a_step, bd + b_step, idesc, 1u);
                     tc_mma<CG>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, idesc, 1u);
                     tc_mma<CG>(d_tmem, ad + 3 * a_step, bd + 3 * b_step, idesc, 1u);
                     if (two) {
-                        ad = a_desc0 + static_cast<uint64_t>(s1) * (C::STAGE_BYTES >> 4);
-                        bd = b_desc0 + static_cast<uint64_t>(s1) * (C::STAGE_BYTES >> 4);
+                        ad = a_desc0 + static_cast<uint64_t>(s1) * (stage_bytes >> 4);
+                        bd = b_desc0 + static_cast<uint64_t>(s1) * (stage_bytes >> 4);
                         tc_mma<CG>(d_tmem, ad, bd, idesc, 1u);
                         tc_mma<CG>(d_tmem, ad + a_step, bd + b_step, idesc, 1u);
                         tc_mma<CG>(d_tmem, ad + 2 * a_step, bd + 2 * b_step, idesc, 1u);
@@ -1009,7 +1026,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     tc_commit<CG>(empty0 + 8u * static_cast<uint32_t>(s0));  // frees the stages (both CTAs)
                     if (two) tc_commit<CG>(empty0 + 8u * static_cast<uint32_t>(s1));
                     if (two) {
-                        stage = s1 + 1 == C::STAGES ? 0 : s1 + 1;
+                        stage = s1 + 1 == stages ? 0 : s1 + 1;
                         phase = stage == 0 ? p1 ^ 1u : p1;
                     } else {
                         stage = s1;
@@ -1946,7 +1963,9 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
         ok = encode_2d(&map_a, dt, p.A, p.M, p.K, p.lda, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
     if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N; box 64 K x B_ROWS
-        ok = encode_2d(&map_b, dt, p.B, p.K, p.N, p.ldb, BK, C::B_ROWS);
+        // (single CTAs: bn1 rows)
+        ok = encode_2d(&map_b, dt, p.B, p.K, p.N, p.ldb, BK,
+                       CG == 1 ? static_cast<uint32_t>(a0.bn1) : C::B_ROWS);
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
         ok = encode_2d(&map_b, dt, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
@@ -2044,6 +2063,9 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.ws = nullptr;
     a.ws_count = nullptr;
     a.cluster_k = 0;
+    a.bn1 = BN;
+    a.stages1 = Cfg<1>::STAGES;
+    a.stage_bytes1 = Cfg<1>::STAGE_BYTES;
     a.ab_format = bf16 ? 1 : 0;
 
     // CTA pairs when there are at least as many 256 x 256 tiles as resident
@@ -2151,6 +2173,16 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             *name = kNames[bf16 ? 1 : 0][ks];  // xN: the K range split over N CTAs
         } else {
             *name = bf16 ? "gemm_bf16_tc" : "gemm_f16_tc";
+        }
+        // N <= 128: one tile column with a 64- or 128-row B box and N = 64
+        // or 128 MMAs, so a stage carries less of B's zero fill past N and
+        // the ring holds 8 or 6 stages instead of 4 -- more of A in flight
+        // when A is the stream (16384 x 64 x 8192)
+        if (p.N <= BN / 2) {
+            a.bn1 = p.N <= BN / 4 ? BN / 4 : BN / 2;
+            a.stage_bytes1 = static_cast<uint32_t>(Cfg<1>::A_BYTES + a.bn1 * BK * 2);
+            const int fit = static_cast<int>(Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES / a.stage_bytes1);
+            a.stages1 = fit < Cfg<1>::MAX_STAGES ? fit : Cfg<1>::MAX_STAGES;
         }
         const int64_t items = tiles * ks;
         const int grid = static_cast<int>(items < d->sms ? items : d->sms);

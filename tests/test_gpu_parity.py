@@ -184,6 +184,30 @@ def test_tc_cluster_split_sizes_full(shape):
         assert np.array_equal(logical_d(w, D2), D)
 
 
+# N <= 128 (after the column-major normalisation): single CTAs take a 64- or
+# 128-row B box and N = 64 / 128 MMAs, with the ring cut into 8 or 6
+# stages; with few tiles the K range is split over a cluster as well.
+# Both B orders (K-contiguous: one narrow box; N-contiguous: one or two
+# 64-column boxes), N at and around the box widths, ragged M and K.
+NARROW_N_SHAPES = [
+    (1000, 64, 777), (1000, 65, 300), (1000, 128, 520), (2000, 33, 1000), (700, 1, 256),
+    (300, 100, 2048),  # 3 tiles: split-K over a cluster with the narrow box
+]
+
+
+@pytest.mark.parametrize("b_order", [COL, ROW])
+@pytest.mark.parametrize("shape", NARROW_N_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in NARROW_N_SHAPES])
+def test_tc_narrow_n_tiles_full(shape, b_order):
+    M, N, K = shape
+    w = Workload("tc_narrow", M, N, K, 1.5, -0.25, "bf16", ROW, b_order, ROW)
+    inp = make_inputs(w, seed=M + 3 * N + K, ld_multiple=8)
+    full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc")
+    # deterministic: a second call gives the same bits
+    D1, _, _ = run_gpu(w, inp)
+    D2, _, _ = run_gpu(w, inp)
+    assert torch.equal(D1, D2)
+
+
 @pytest.mark.parametrize("orders", [(ROW, COL, ROW), (COL, ROW, COL)])
 def test_f16_pair_and_split_variants_full(orders):
     for shape, kernel in [(PAIR_SHAPE, "gemm_f16_tc<pair"), (TC_SPLIT_SHAPE, "gemm_f16_tc<splitk,")]:
