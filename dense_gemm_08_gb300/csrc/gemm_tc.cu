@@ -160,6 +160,10 @@ struct TcArgs {
     int bn1;
     int stages1;
     uint32_t stage_bytes1;
+    // CG = 1: rows of A loaded per stage (BM, or 16 / 32 / 64 when M fits:
+    // the rows past them in shared memory hold stale values, which reach
+    // only accumulator rows past M -- rows of D that are never stored)
+    int am1;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -876,7 +880,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 const int32_t m0 = static_cast<int32_t>(tm * C::TILE_M + rank * BM);
                 const int b_rows = it.n_width / CG;  // columns of B this CTA loads
                 const int32_t n0 = static_cast<int32_t>(tn * BN + it.n_off + rank * b_rows);
-                const uint32_t stage_tx = CG * (C::A_BYTES + b_rows * BK * 2);
+                const int a_rows = CG == 1 ? args.am1 : BM;  // rows of A this stage loads
+                const uint32_t stage_tx = CG * (a_rows * BK * 2 + b_rows * BK * 2);
                 // Serpentine K order: every other work item walks its K blocks
                 // backwards, so the blocks a round of tiles reads last are the
                 // ones the next round (the same tile rows, under the grouped
@@ -884,8 +889,15 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 // side takes the stages as they come (the sum's order changes,
                 // not its terms).
                 const bool reverse = (li & 1) != 0;
-                for (int64_t i = 0; i < it.kb_end - it.kb_begin; ++i) {
-                    const int64_t kb = reverse ? it.kb_end - 1 - i : it.kb_begin + i;
+                // Single-CTA tiles with M <= 64 share A's K blocks, a few
+                // lines each: each tile starts its K range at a different
+                // block, so the CTAs do not all read the same lines at once.
+                const int64_t nkb = it.kb_end - it.kb_begin;
+                const int64_t rot = (CG == 1 && args.am1 < BM && nkb > 1) ? it.t % nkb : 0;
+                for (int64_t i = 0; i < nkb; ++i) {
+                    int64_t j = (reverse ? nkb - 1 - i : i) + rot;
+                    if (j >= nkb) j -= nkb;
+                    const int64_t kb = it.kb_begin + j;
                     if (!wait_bounded(smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                       args.timeout_ns)) {
                         raise_abort(abort_flag);
@@ -902,7 +914,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     if (args.a_kmajor) {
                         tma_load_2d<CG>(sa, &map_a, k0, m0, fb);
                     } else {
-                        for (int i = 0; i < BM / 64; ++i)
+                        for (int i = 0; i < a_rows / 64; ++i)
                             tma_load_2d<CG>(sa + i * 64 * 128, &map_a, m0 + 64 * i, k0, fb);
                     }
                     if (args.b_kmajor) {
@@ -1958,7 +1970,9 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
         a0.ab_format == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     bool ok;
     if (p.a_kmajor)  // A(i, k) at A[i * lda + k]: inner K, outer M; box 64 K x 128 rows
-        ok = encode_2d(&map_a, dt, p.A, p.K, p.M, p.lda, BK, BM);
+        // (single CTAs: am1 rows)
+        ok = encode_2d(&map_a, dt, p.A, p.K, p.M, p.lda, BK,
+                       CG == 1 ? static_cast<uint32_t>(a0.am1) : BM);
     else  // A(i, k) at A[i + k * lda]: inner M, outer K; boxes of 64 M x 64 K
         ok = encode_2d(&map_a, dt, p.A, p.M, p.K, p.lda, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
@@ -2064,6 +2078,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.ws_count = nullptr;
     a.cluster_k = 0;
     a.bn1 = BN;
+    a.am1 = BM;
     a.stages1 = Cfg<1>::STAGES;
     a.stage_bytes1 = Cfg<1>::STAGE_BYTES;
     a.ab_format = bf16 ? 1 : 0;
@@ -2178,6 +2193,10 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         // or 128 MMAs, so a stage carries less of B's zero fill past N and
         // the ring holds 8 or 6 stages instead of 4 -- more of A in flight
         // when A is the stream (16384 x 64 x 8192)
+        // M <= 64: load only the rows of A that hold data (at least 16 for a
+        // K-major A, 64 -- one box -- for an M-major one); TMA then moves
+        // fewer zero-filled rows per stage
+        if (p.M <= 64) a.am1 = p.a_kmajor ? (p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64)) : 64;
         if (p.N <= BN / 2) {
             a.bn1 = p.N <= BN / 4 ? BN / 4 : BN / 2;
             a.stage_bytes1 = static_cast<uint32_t>(Cfg<1>::A_BYTES + a.bn1 * BK * 2);
