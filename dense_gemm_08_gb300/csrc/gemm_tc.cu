@@ -162,8 +162,11 @@ struct TcArgs {
     uint32_t stage_bytes1;
     // CG = 1: rows of A loaded per stage (BM, or 16 / 32 / 64 when M fits:
     // the rows past them in shared memory hold stale values, which reach
-    // only accumulator rows past M -- rows of D that are never stored)
+    // only accumulator rows past M -- rows of D that are never stored), and
+    // likewise rows of a K-contiguous B (bn1, or 16 / 32 when N fits; the
+    // stale rows reach only columns past N)
     int am1;
+    int bk1;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -881,7 +884,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                 const int b_rows = it.n_width / CG;  // columns of B this CTA loads
                 const int32_t n0 = static_cast<int32_t>(tn * BN + it.n_off + rank * b_rows);
                 const int a_rows = CG == 1 ? args.am1 : BM;  // rows of A this stage loads
-                const uint32_t stage_tx = CG * (a_rows * BK * 2 + b_rows * BK * 2);
+                const int b_load = (CG == 1 && args.b_kmajor) ? args.bk1 : b_rows;  // and of B
+                const uint32_t stage_tx = CG * (a_rows * BK * 2 + b_load * BK * 2);
                 // Serpentine K order: every other work item walks its K blocks
                 // backwards, so the blocks a round of tiles reads last are the
                 // ones the next round (the same tile rows, under the grouped
@@ -1979,7 +1983,7 @@ cudaError_t launch_variant(const Problem &p, const TcArgs &a0, int grid, cudaStr
     if (p.b_kmajor)  // B(k, j) at B[k + j * ldb]: inner K, outer N; box 64 K x B_ROWS
         // (single CTAs: bn1 rows)
         ok = encode_2d(&map_b, dt, p.B, p.K, p.N, p.ldb, BK,
-                       CG == 1 ? static_cast<uint32_t>(a0.bn1) : C::B_ROWS);
+                       CG == 1 ? static_cast<uint32_t>(a0.bk1) : C::B_ROWS);
     else  // B(k, j) at B[k * ldb + j]: inner N, outer K; boxes of 64 N x 64 K
         ok = encode_2d(&map_b, dt, p.B, p.N, p.K, p.ldb, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
@@ -2079,6 +2083,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.cluster_k = 0;
     a.bn1 = BN;
     a.am1 = BM;
+    a.bk1 = BN;
     a.stages1 = Cfg<1>::STAGES;
     a.stage_bytes1 = Cfg<1>::STAGE_BYTES;
     a.ab_format = bf16 ? 1 : 0;
@@ -2199,6 +2204,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         if (p.M <= 64) a.am1 = p.a_kmajor ? (p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64)) : 64;
         if (p.N <= BN / 2) {
             a.bn1 = p.N <= BN / 4 ? BN / 4 : BN / 2;
+            a.bk1 = p.N <= 16 ? 16 : (p.N <= 32 ? 32 : a.bn1);
             a.stage_bytes1 = static_cast<uint32_t>(Cfg<1>::A_BYTES + a.bn1 * BK * 2);
             const int fit = static_cast<int>(Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES / a.stage_bytes1);
             a.stages1 = fit < Cfg<1>::MAX_STAGES ? fit : Cfg<1>::MAX_STAGES;

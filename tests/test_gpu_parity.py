@@ -191,7 +191,11 @@ def test_tc_cluster_split_sizes_full(shape):
 # 64-column boxes), N at and around the box widths, ragged M and K.
 NARROW_N_SHAPES = [
     (1000, 64, 777), (1000, 65, 300), (1000, 128, 520), (2000, 33, 1000), (700, 1, 256),
+    # N <= 32 with a K-contiguous B: 16 or 32 rows of B per stage, the
+    # other rows stale (they reach only columns past N)
+    (1500, 7, 600), (1500, 16, 600), (1500, 17, 600), (1500, 32, 600),
     (300, 100, 2048),  # 3 tiles: split-K over a cluster with the narrow box
+    (200, 9, 3000),  # 2 tiles: split-K with a 16-row B box
 ]
 
 
@@ -206,6 +210,22 @@ def test_tc_narrow_n_tiles_full(shape, b_order):
     D1, _, _ = run_gpu(w, inp)
     D2, _, _ = run_gpu(w, inp)
     assert torch.equal(D1, D2)
+
+
+# M <= 64: single CTAs load 16, 32 or 64 rows of a K-contiguous A (one
+# 64-row box of an M-contiguous A); the tile's other rows hold stale shared
+# memory and must not reach D.  M at and around each box height, both A
+# orders, with and without the cluster split-K, beta != 0 (C read).
+SMALL_M = [1, 7, 16, 17, 32, 33, 64]
+
+
+@pytest.mark.parametrize("a_order", [ROW, COL])
+@pytest.mark.parametrize("M", SMALL_M)
+def test_tc_small_m_a_box_full(M, a_order):
+    for N, K in [(600, 1000), (2000, 96)]:  # split over a cluster; K = 96: no split
+        w = Workload("tc_small_m", M, N, K, 1.5, -0.25, "bf16", a_order, COL, ROW)
+        inp = make_inputs(w, seed=M * 7 + N + K, ld_multiple=8)
+        full_check(w, inp, pad_d=3, expect_kernel="gemm_bf16_tc")
 
 
 @pytest.mark.parametrize("orders", [(ROW, COL, ROW), (COL, ROW, COL)])
