@@ -167,6 +167,10 @@ struct TcArgs {
     // stale rows reach only columns past N)
     int am1;
     int bk1;
+    // CG = 1: bytes of A at the start of each stage, B after them (BM rows,
+    // or am1 rows packed tight: the MMA's 128-row A operand then runs on
+    // into B and the next stage, stale rows that reach only rows past M)
+    uint32_t a_region1;
     int ab_format;  // operand format of A and B for kind::f16: 1 = BF16, 0 = FP16
     // fused epilogue: D = act(alpha * acc + beta * C + bias), FP32 or BF16
     const float *bias;
@@ -866,6 +870,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     // ring stages (compile-time for CTA pairs)
     const int stages = CG == 1 ? args.stages1 : C::STAGES;
     const uint32_t stage_bytes = CG == 1 ? args.stage_bytes1 : C::STAGE_BYTES;
+    const uint32_t a_region = CG == 1 ? args.a_region1 : C::A_BYTES;  // B starts here in a stage
     bool aborted = false;
 
     if (warp == 0) {
@@ -912,7 +917,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
                     // the leader's full barrier counts both CTAs' bytes
                     const uint32_t fb = CG == 1 ? fb_local : map_to_rank(fb_local, 0);
                     const uint32_t sa = ring_base + stage * stage_bytes;
-                    const uint32_t sb = sa + C::A_BYTES;
+                    const uint32_t sb = sa + a_region;
                     const int32_t k0 = static_cast<int32_t>(kb * BK);
                     if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
                     if (args.a_kmajor) {
@@ -983,8 +988,8 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
             // their 8 MMAs back to back.
             const uint32_t full0 = smem_addr(&full[0]), empty0 = smem_addr(&empty[0]);
             const uint64_t a_desc0 = args.a_kmajor ? desc_kmajor(ring_base, 0) : desc_mnmajor(ring_base, 0);
-            const uint64_t b_desc0 = args.b_kmajor ? desc_kmajor(ring_base + C::A_BYTES, 0)
-                                                   : desc_mnmajor(ring_base + C::A_BYTES, 0);
+            const uint64_t b_desc0 = args.b_kmajor ? desc_kmajor(ring_base + a_region, 0)
+                                                   : desc_mnmajor(ring_base + a_region, 0);
             const uint64_t a_step = args.a_kmajor ? (UMMA_K * 2) >> 4 : (UMMA_K * 128) >> 4;
             const uint64_t b_step = args.b_kmajor ? (UMMA_K * 2) >> 4 : (UMMA_K * 128) >> 4;
             for (int64_t w = group_id; w < n_items && ok; w += num_groups, ++li) {
@@ -2084,6 +2089,7 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
     a.bn1 = BN;
     a.am1 = BM;
     a.bk1 = BN;
+    a.a_region1 = Cfg<1>::A_BYTES;
     a.stages1 = Cfg<1>::STAGES;
     a.stage_bytes1 = Cfg<1>::STAGE_BYTES;
     a.ab_format = bf16 ? 1 : 0;
@@ -2205,10 +2211,13 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         if (p.N <= BN / 2) {
             a.bn1 = p.N <= BN / 4 ? BN / 4 : BN / 2;
             a.bk1 = p.N <= 16 ? 16 : (p.N <= 32 ? 32 : a.bn1);
-            a.stage_bytes1 = static_cast<uint32_t>(Cfg<1>::A_BYTES + a.bn1 * BK * 2);
-            const int fit = static_cast<int>(Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES / a.stage_bytes1);
-            a.stages1 = fit < Cfg<1>::MAX_STAGES ? fit : Cfg<1>::MAX_STAGES;
         }
+        // stages packed tight: A's loaded rows, then the bn1 rows of B the
+        // MMAs read; as many as the ring holds, at most MAX_STAGES
+        a.a_region1 = static_cast<uint32_t>(a.am1 * BK * 2);
+        a.stage_bytes1 = a.a_region1 + static_cast<uint32_t>(a.bn1 * BK * 2);
+        const int fit = static_cast<int>(Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES / a.stage_bytes1);
+        a.stages1 = fit < Cfg<1>::MAX_STAGES ? fit : Cfg<1>::MAX_STAGES;
         const int64_t items = tiles * ks;
         const int grid = static_cast<int>(items < d->sms ? items : d->sms);
         e = launch_variant<1>(p, a, grid, stream);
