@@ -69,6 +69,15 @@ constexpr int kGroupM = 16;               // grouped raster width (tile rows)
 #ifndef GEMM_TC_DIRECT_STAGES
 #define GEMM_TC_DIRECT_STAGES 7
 #endif
+// Debug build (-DGEMM_TC_DEBUG=1): every ring at its smallest depth (2
+// stages, the fewest the MMA loop's two-stage rounds take) and a grid of one
+// work item per CTA (or pair) instead of the persistent one, so that a wrong
+// result can be told apart from a ring or phase mistake.  Same results
+// contract; for checking, not for speed.
+#ifndef GEMM_TC_DEBUG
+#define GEMM_TC_DEBUG 0
+#endif
+constexpr bool kDebug = GEMM_TC_DEBUG != 0;
 static_assert(GEMM_TC_PAIR_STAGES >= 2 && GEMM_TC_PAIR_STAGES <= 5,
               "the staged pair ring holds 2 to 5 stages");
 static_assert(GEMM_TC_DIRECT_STAGES >= 2 && GEMM_TC_DIRECT_STAGES <= 7,
@@ -87,8 +96,10 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // (the debug build keeps the same shared-memory layout, using 2 stages)
     static constexpr int STAGES =
         CG == 1 ? 4 : (DIRECT ? GEMM_TC_DIRECT_STAGES : GEMM_TC_PAIR_STAGES);
+    static constexpr int RING_STAGES = kDebug ? 2 : STAGES;  // stages the ring cycles through
     // single CTAs with a narrow B tile (N <= 128: 64 or 128 rows of B per
     // stage) cut the same ring into more, smaller stages, at most 8
     static constexpr int MAX_STAGES = CG == 1 ? 8 : STAGES;
@@ -868,7 +879,7 @@ __global__ void __launch_bounds__(Cfg<CG, DIRECT>::THREADS, 1)
     const int64_t n_items = work_items<CG>(args);
     const uint32_t ring_base = smem_addr(ring);
     // ring stages (compile-time for CTA pairs)
-    const int stages = CG == 1 ? args.stages1 : C::STAGES;
+    const int stages = CG == 1 ? args.stages1 : C::RING_STAGES;
     const uint32_t stage_bytes = CG == 1 ? args.stage_bytes1 : C::STAGE_BYTES;
     const uint32_t a_region = CG == 1 ? args.a_region1 : C::A_BYTES;  // B starts here in a stage
     bool aborted = false;
@@ -2161,8 +2172,11 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
             if (e != cudaSuccess) return e;
             a.ws = static_cast<float *>(ws);
         }
-        e = direct ? launch_variant<2, true>(p, a, 2 * pairs, stream)
-                   : launch_variant<2, false>(p, a, 2 * pairs, stream);
+        // (debug: one work item per pair)
+        const int64_t pair_items = a.tail_first + (pair_tiles - a.tail_first) * a.tail_ks;
+        const int grid2 = static_cast<int>(kDebug ? 2 * pair_items : 2 * pairs);
+        e = direct ? launch_variant<2, true>(p, a, grid2, stream)
+                   : launch_variant<2, false>(p, a, grid2, stream);
         if (ws != nullptr) {
             const cudaError_t ef = workspace_free(ws, stream);
             if (e == cudaSuccess) e = ef;
@@ -2218,8 +2232,10 @@ cudaError_t launch_tc(const Problem &p, InType in, cudaStream_t stream, const ch
         a.stage_bytes1 = a.a_region1 + static_cast<uint32_t>(a.bn1 * BK * 2);
         const int fit = static_cast<int>(Cfg<1>::STAGES * Cfg<1>::STAGE_BYTES / a.stage_bytes1);
         a.stages1 = fit < Cfg<1>::MAX_STAGES ? fit : Cfg<1>::MAX_STAGES;
+        if (kDebug) a.stages1 = 2;
         const int64_t items = tiles * ks;
-        const int grid = static_cast<int>(items < d->sms ? items : d->sms);
+        // (debug: one item per CTA; items < 2^31 by the tile bound above)
+        const int grid = static_cast<int>(kDebug || items < d->sms ? items : d->sms);
         e = launch_variant<1>(p, a, grid, stream);
     }
     if (e != cudaSuccess) return e;
