@@ -81,13 +81,16 @@ def test_epilogue_tensor_core_moderate(act, d_type, with_bias):
 
 
 @pytest.mark.parametrize("variant", ["pair", "pair_staged", "pair_tail", "splitk", "simt",
-                                     "scale_c", "col_major_d", "unaligned_d", "ragged_n"])
+                                     "scale_c", "col_major_d", "unaligned_d", "ragged_n",
+                                     "narrow_n", "small_m"])
 @pytest.mark.parametrize("d_type", DTYPES)
 def test_epilogue_every_path(variant, d_type):
     shapes = {"pair": (2500, 2600, 136), "pair_staged": (2500, 2600, 136),
               "pair_tail": (2000, 3300, 777), "splitk": (300, 600, 2048), "simt": (150, 270, 101),
               "scale_c": (70, 90, 0), "col_major_d": (300, 600, 200), "unaligned_d": (300, 601, 200),
-              "ragged_n": (300, 601, 200)}
+              "ragged_n": (300, 601, 200),
+              # single CTAs: a 64-row B box (N = 48), a 16-row A box (M = 5)
+              "narrow_n": (1000, 48, 700), "small_m": (5, 600, 1000)}
     M, N, K = shapes[variant]
     order_cd = COL if variant == "col_major_d" else ROW
     w = Workload("epi_" + variant, M, N, K, 1.5, -0.25, "bf16", ROW, COL, order_cd)
@@ -97,7 +100,8 @@ def test_epilogue_every_path(variant, d_type):
               "pair_tail": "gemm_bf16_tc<pair",
               "splitk": "gemm_bf16_tc<splitk,",
               "simt": "sgemm_simt<bf16", "scale_c": "scale_c", "col_major_d": "gemm_bf16_tc",
-              "unaligned_d": "gemm_bf16_tc", "ragged_n": "gemm_bf16_tc"}[variant]
+              "unaligned_d": "gemm_bf16_tc", "ragged_n": "gemm_bf16_tc",
+              "narrow_n": "gemm_bf16_tc", "small_m": "gemm_bf16_tc<splitk,x"}[variant]
     # D rows on 32 bytes (the pair kernel's direct epilogue; TMA stores on the
     # single-CTA kernel) except: pair_staged has 16-byte rows (2604, staged
     # boxes and TMA stores), unaligned_d an odd ldd (603), and ragged_n a
